@@ -1,0 +1,251 @@
+"""CPU oracle for the USP (Ulysses x Ring) attention step -- TEST INFRASTRUCTURE.
+
+This is the slow, plain, obviously-correct statement of what the CUDA path
+computes.  Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s
+CPU-baseline leg may import or call it; the library never does.  It shares no
+code with the CUDA path.  Floating point is fp64 throughout: inputs stored as
+bf16 or fp32 are widened exactly before any arithmetic.
+
+Sources (page titles as extracted):
+
+* [HB]  "Multi-GPU parallelism: spreading one step over several cards",
+  section "Sequence parallelism: Ulysses and Ring" -- the four-card Ulysses
+  simulation (per-card token slices, ``all_to_all_heads``, per-card SDPA,
+  ``all_to_all_tokens``) and the statement that Ring merges the per-block
+  local results with a log-sum-exp, the formula of FlashAttention's online
+  softmax; the figure caption there: K and V blocks are "passed station by
+  station" around the ring.
+* [PR]  "Feat: USP sequence parallelism (Ulysses x Ring) via
+  SequenceParallelPlan; Wan enabled", Design, "Coordinates" (sp = ulysses x
+  ring, Ulysses ranks contiguous, ring ranks strided), "Ring kernel
+  selection" (kernels return LSE and pair with a real backward), Numerics.
+* [VO]  vllm-omni "Parallelism Acceleration Guide", "How to parallelize a new
+  model": tokens are chunked along the sequence by SP rank in rank order.
+
+Readings where the pages are silent or open:
+
+* LSE is the natural-log log-sum-exp of the scaled scores, one value per
+  (b, h, query row).
+* The merge is the standard log-sum-exp combination (the pages name it but do
+  not print it): m = max_t lse_t; L = m + ln sum_t exp(lse_t - m);
+  O = sum_t exp(lse_t - L) O_t.
+* At ring step t, ring rank g holds KV chunk c = (g - t) mod ring
+  ("passed station by station"); the merged result does not depend on the
+  order up to rounding.
+* Virtual rank (g, j) has sp_rank = g * ulysses + j; its tokens are
+  [sp_rank*Ns, (sp_rank+1)*Ns); Ulysses rank j owns heads
+  [j*Hu, (j+1)*Hu); the head-sharded buffer concatenates the u source ranks
+  of its ring group in rank order along tokens.
+* No mask, no causal masking, no dropout; an explicit ``scale`` (1/sqrt(D)
+  in every workload, SDPA's default).
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against
+library routines (torch fp64 SDPA and autograd on CPU), closed forms,
+invariants and brute force; none is marked "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# Ulysses all-to-all as an index re-layout  ([HB] all_to_all_heads / _tokens)
+# ---------------------------------------------------------------------------
+
+def tok2head(T: np.ndarray, ulysses: int, ring: int) -> np.ndarray:
+    """Token-sharded stack -> head-sharded stack.
+
+    T has shape [ring, ulysses, B, H, Ns, *tail] (tail = (D,) for q/k/v/O,
+    () for LSE).  The result X has shape [ring, ulysses, B, H/u, u*Ns, *tail]
+    with, for every index,
+
+        X[g, j, b, h', s*Ns + n', ...] = T[g, s, b, j*Hu + h', n', ...]
+
+    i.e. destination Ulysses rank j gathers head group j from every source
+    rank s of its ring group and concatenates them by token in source-rank
+    order ([HB], ``all_to_all_heads``).  Pure indexing: the element type is
+    untouched (pass a uint16 view for bf16 data).
+    """
+    r, u, B, H, Ns = T.shape[:5]
+    assert r == ring and u == ulysses and H % u == 0
+    Hu = H // u
+    X = np.empty((r, u, B, Hu, u * Ns) + T.shape[5:], dtype=T.dtype)
+    for g in range(r):
+        for j in range(u):              # destination Ulysses rank
+            for s in range(u):          # source Ulysses rank, in rank order
+                X[g, j, :, :, s * Ns:(s + 1) * Ns] = T[g, s, :, j * Hu:(j + 1) * Hu]
+    return X
+
+
+def head2tok(X: np.ndarray, ulysses: int, ring: int) -> np.ndarray:
+    """Head-sharded stack -> token-sharded stack (inverse of :func:`tok2head`).
+
+        T[g, s, b, j*Hu + h', n', ...] = X[g, j, b, h', s*Ns + n', ...]
+
+    Destination rank s collects its own token slice from every head group j
+    and concatenates along heads in rank order ([HB], ``all_to_all_tokens``).
+    """
+    r, u, B, Hu, Nr = X.shape[:5]
+    assert r == ring and u == ulysses and Nr % u == 0
+    Ns = Nr // u
+    T = np.empty((r, u, B, Hu * u, Ns) + X.shape[5:], dtype=X.dtype)
+    for g in range(r):
+        for s in range(u):              # destination (token) rank
+            for j in range(u):          # source head group, in rank order
+                T[g, s, :, j * Hu:(j + 1) * Hu] = X[g, j, :, :, s * Ns:(s + 1) * Ns]
+    return T
+
+
+# ---------------------------------------------------------------------------
+# Chunk attention returning the log-sum-exp ([HB] per-card SDPA; [PR] LSE)
+# ---------------------------------------------------------------------------
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
+              row_block: int = 1024):
+    """O = softmax(scale * q k^T) v and lse = ln sum_j exp(scale * q k^T)_ij.
+
+    q: [..., Nq, D], k and v: [..., Nk, D] (any leading batch dims, equal
+    for all three).  Computed in fp64 in two passes over each row:
+      pass 1: S = scale * q k^T, m = max_j S_ij, lse = m + ln sum_j exp(S_ij - m)
+      pass 2: O = exp(S - lse) v
+    Rows are evaluated ``row_block`` at a time only to bound memory; every
+    row is independent, so this changes no arithmetic.
+    Returns (O [..., Nq, D] fp64, lse [..., Nq] fp64).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    Nq = q.shape[-2]
+    O = np.empty(q.shape[:-1] + (v.shape[-1],), dtype=np.float64)
+    L = np.empty(q.shape[:-1], dtype=np.float64)
+    kT = np.swapaxes(k, -1, -2)
+    for r0 in range(0, Nq, row_block):
+        r1 = min(Nq, r0 + row_block)
+        S = scale * (q[..., r0:r1, :] @ kT)                 # [..., rows, Nk]
+        m = S.max(axis=-1, keepdims=True)                   # pass 1: row max
+        lse = m[..., 0] + np.log(np.exp(S - m).sum(axis=-1))  # pass 1: exp-sum
+        O[..., r0:r1, :] = np.exp(S - lse[..., None]) @ v   # pass 2
+        L[..., r0:r1] = lse
+    return O, L
+
+
+def attention_rows(q, k, v, rows, scale: float, row_block: int = 1024):
+    """:func:`attention` for the query rows ``rows`` only (index along Nq)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    return attention(np.asarray(q)[..., rows, :], k, v, scale, row_block)
+
+
+# ---------------------------------------------------------------------------
+# Ring step: log-sum-exp merge of partial results ([HB] Ring paragraph)
+# ---------------------------------------------------------------------------
+
+def lse_merge(outs: np.ndarray, lses: np.ndarray):
+    """Merge R partial attentions over disjoint KV chunks.
+
+    outs: [R, ..., Nq, D], lses: [R, ..., Nq] (partial t attended to KV chunk
+    t only).  Two passes, fp64:
+      pass 1: m = max_t lse_t;  L = m + ln sum_t exp(lse_t - m)
+      pass 2: O = sum_t exp(lse_t - L) * O_t
+    Returns (O [..., Nq, D], L [..., Nq]).
+    """
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    m = lses.max(axis=0)
+    L = m + np.log(np.exp(lses - m[None]).sum(axis=0))
+    O = np.zeros(outs.shape[1:], dtype=np.float64)
+    for t in range(outs.shape[0]):
+        O += np.exp(lses[t] - L)[..., None] * outs[t]
+    return O, L
+
+
+# ---------------------------------------------------------------------------
+# The USP simulation: Ulysses re-layout, ring steps, merge, re-layout back
+# ---------------------------------------------------------------------------
+
+def ring_chunk(g: int, t: int, ring: int) -> int:
+    """KV chunk held by ring rank g at ring step t (t = 0: its own chunk)."""
+    return (g - t) % ring
+
+
+def usp_forward(Tq, Tk, Tv, ulysses: int, ring: int, scale: float):
+    """USP attention forward on token-sharded stacks, as the pages simulate it.
+
+    Tq/Tk/Tv: [ring, ulysses, B, H, Ns, D] (any float dtype; widened to fp64).
+    Steps ([HB] simulation extended by the Ring paragraph and [PR] Design):
+      1. tok2head on q, k, v (Ulysses all-to-all);
+      2. for every virtual rank (g, j) and ring step t = 0..ring-1, attention
+         of its queries against KV chunk c = (g - t) mod ring, returning
+         (O_t, lse_t);
+      3. log-sum-exp merge over t;
+      4. head2tok on O and on the LSE.
+    Returns (O [ring, ulysses, B, H, Ns, D], LSE [ring, ulysses, B, H, Ns]).
+    """
+    Xq = tok2head(np.asarray(Tq, dtype=np.float64), ulysses, ring)
+    Xk = tok2head(np.asarray(Tk, dtype=np.float64), ulysses, ring)
+    Xv = tok2head(np.asarray(Tv, dtype=np.float64), ulysses, ring)
+    parts_o = np.empty((ring,) + Xq.shape, dtype=np.float64)
+    parts_l = np.empty((ring,) + Xq.shape[:-1], dtype=np.float64)
+    for g in range(ring):
+        for j in range(ulysses):
+            for t in range(ring):
+                c = ring_chunk(g, t, ring)
+                parts_o[t, g, j], parts_l[t, g, j] = attention(Xq[g, j], Xk[c, j], Xv[c, j], scale)
+    Xo, Xl = lse_merge(parts_o, parts_l)
+    return head2tok(Xo, ulysses, ring), head2tok(Xl, ulysses, ring)
+
+
+# ---------------------------------------------------------------------------
+# Backward ([PR] Ring kernel selection: LSE paired with a real backward)
+# ---------------------------------------------------------------------------
+
+def attention_bwd(q, k, v, o, lse, dout, scale: float):
+    """Gradients of O = softmax(scale q k^T) v for one or more heads, fp64.
+
+    With P = exp(scale q k^T - lse):
+      dV = P^T dO;  dP = dO V^T;  Delta_i = sum_d dO_id O_id;
+      dS = P * (dP - Delta);  dQ = scale dS K;  dK = scale dS^T Q.
+    ``o`` and ``lse`` are the forward outputs (the oracle's own).
+    Returns (dq, dk, dv) in fp64.
+    """
+    q, k, v, o, lse, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, o, lse, dout))
+    P = np.exp(scale * (q @ np.swapaxes(k, -1, -2)) - lse[..., None])
+    dv = np.swapaxes(P, -1, -2) @ dout
+    dP = dout @ np.swapaxes(v, -1, -2)
+    delta = (dout * o).sum(axis=-1)
+    dS = P * (dP - delta[..., None])
+    dq = scale * (dS @ k)
+    dk = scale * (np.swapaxes(dS, -1, -2) @ q)
+    return dq, dk, dv
+
+
+def attention_bwd_sampled(q, k, v, dout, scale: float, qrows, krows, row_block: int = 1024):
+    """Backward of one head at sampled rows, exact in fp64.
+
+    q, k, v, dout: [N, D] for one (b, h).  Computes the forward O and lse
+    for ALL rows (needed for Delta and for every P column), then dq at the
+    query rows ``qrows`` and dk, dv at the key rows ``krows`` from the same
+    formulas as :func:`attention_bwd`, column by column.
+    Returns (dq [len(qrows), D], dk [len(krows), D], dv [len(krows), D]).
+    """
+    q, k, v, dout = (np.asarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    o, lse = attention(q, k, v, scale, row_block)
+    delta = (dout * o).sum(axis=-1)
+    qrows = np.asarray(qrows, dtype=np.int64)
+    krows = np.asarray(krows, dtype=np.int64)
+    # dq rows: full P and dP rows for the sampled queries
+    Pq = np.exp(scale * (q[qrows] @ k.T) - lse[qrows, None])
+    dPq = dout[qrows] @ v.T
+    dq = scale * ((Pq * (dPq - delta[qrows, None])) @ k)
+    # dk, dv rows: full P and dP columns for the sampled keys
+    N = q.shape[0]
+    dk = np.zeros((len(krows), k.shape[1]))
+    dv = np.zeros((len(krows), v.shape[1]))
+    kS, vS = k[krows], v[krows]
+    for r0 in range(0, N, row_block):
+        r1 = min(N, r0 + row_block)
+        Pc = np.exp(scale * (q[r0:r1] @ kS.T) - lse[r0:r1, None])      # [rows, |krows|]
+        dPc = dout[r0:r1] @ vS.T
+        dSc = Pc * (dPc - delta[r0:r1, None])
+        dv += Pc.T @ dout[r0:r1]
+        dk += scale * (dSc.T @ q[r0:r1])
+    return dq, dk, dv
