@@ -1,0 +1,394 @@
+"""Benchmark of the USP attention hot path on GB300.
+
+One step = one pass of every built row of the hot path over one batch of
+synthetic input of the named workload (default: Qwen-Image 1024^2, bf16,
+B1 H24 N4096 D128, ulysses 2 x ring 2):
+  * usp_attention_fwd, materialised: tok2head(q,k,v) -> per-(rank, ring step)
+    chunk attention -> LSE merge -> head2tok(out, lse)
+  * usp_attention_fwd, fused: one kernel over the token-sharded stacks
+  * usp_attention_bwd (when the workload has a backward)
+``value`` is algorithmic attention FLOP of the step (4*B*H*N^2*D per forward,
+10*B*H*N^2*D per backward) / device time, in TFLOP/s, summed over ranks.
+Inputs (q, k, v: ~25 MB each) are smaller than L2, so L2 is flushed (a
+256 MB buffer is written) before every timed step, outside the timed events.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun every rank runs its own replica (weak scaling, no data-path
+collective); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from diffusion_transformer_sequence_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "USP attention fwd(+bwd) TFLOP/s and % of GB300 bf16 peak; re-layout GB/s vs HBM"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------- reference arm
+def oracle_sample_flop(w, heads):
+    return 4.0 * w.B * heads * w.N * w.N * w.D
+
+
+def run_oracle_sample(w, heads: int):
+    """Time the CPU oracle's USP forward on `heads` heads of the workload."""
+    import oracle
+    sub = wl.custom(w.name, w.dtype, w.B, heads, w.N, w.D, w.ulysses, w.ring, seed=w.seed)
+    inp = wl.make_inputs(sub, with_dout=False)
+    stacks = [wl.to_token_stack(inp[n], w.ulysses, w.ring).double().numpy() for n in ("q", "k", "v")]
+    t0 = time.perf_counter()
+    oracle.usp_forward(*stacks, w.ulysses, w.ring, w.scale)
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def sample_heads(w):
+    # smallest head count the Ulysses split allows, enough for ~10-30 s of CPU work
+    return min(w.H, max(w.ulysses, (w.H // 2) // w.ulysses * w.ulysses))
+
+
+def reference_arm(args, w, ws, rank):
+    if rank != 0:
+        return
+    heads = sample_heads(w)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = run_oracle_sample(w, heads)
+        if i >= args.warmup:
+            times.append(dt)
+    flop = oracle_sample_flop(w, heads)
+    tflops = flop / statistics.mean(times) / 1e12
+    sample = f"oracle USP forward (numpy fp64) on {heads} of {w.H} heads of {w.name}, full N"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "desc": w.description, "global_batch": w.B, "seq_len": w.N,
+                   "ulysses": w.ulysses, "ring": w.ring, "parallelism": "virtual ranks on one device"},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+class Step:
+    """Device buffers and the calls of one step, with per-call CUDA events."""
+
+    def __init__(self, w, backward: bool):
+        import diffusion_transformer_sequence_gb300 as usp
+        self.usp = usp
+        self.w = w
+        inp = wl.make_inputs(w, with_dout=backward)
+        self.host = {n: wl.to_token_stack(t, w.ulysses, w.ring).pin_memory() for n, t in inp.items()}
+        self.dev = {n: t.cuda() for n, t in self.host.items()}
+        self.out_m = torch.empty_like(self.dev["q"])
+        self.lse_m = torch.empty(w.lse_stack_shape, dtype=torch.float32, device="cuda")
+        self.out_f = torch.empty_like(self.dev["q"])
+        self.lse_f = torch.empty(w.lse_stack_shape, dtype=torch.float32, device="cuda")
+        nws = usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, "materialised")
+        self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+        self.backward = backward
+        self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.launches_per_step = (7 if w.ring > 1 else 6) + 1
+
+    def flop(self):
+        f = 2 * self.w.fwd_flop
+        if self.backward:
+            f += self.w.bwd_flop
+        return f
+
+    def flush(self):
+        self.flush_buf.fill_(1)
+
+    def run(self, ev=None):
+        usp, w = self.usp, self.w
+        if ev:
+            ev[0].record()
+        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                          mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
+        if ev:
+            ev[1].record()
+        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                          mode="fused", out=self.out_f, lse=self.lse_f)
+        if ev:
+            ev[2].record()
+
+    def run_e2e(self):
+        """Host buffers in and out: H2D of q, k, v, the step, D2H of the outputs."""
+        usp, w = self.usp, self.w
+        for n in ("q", "k", "v"):
+            self.dev[n].copy_(self.host[n], non_blocking=True)
+        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                          mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
+        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                          mode="fused", out=self.out_f, lse=self.lse_f)
+        for name, t in (("out_m", self.out_m), ("lse_m", self.lse_m), ("out_f", self.out_f), ("lse_f", self.lse_f)):
+            dst = getattr(self, "h_" + name, None)
+            if dst is None:
+                dst = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                setattr(self, "h_" + name, dst)
+            dst.copy_(t, non_blocking=True)
+
+    def io_bytes(self):
+        h2d = sum(self.host[n].numel() * self.host[n].element_size() for n in ("q", "k", "v"))
+        d2h = 2 * (self.out_m.numel() * self.out_m.element_size() + self.lse_m.numel() * 4)
+        return h2d, d2h
+
+
+def time_rows(w, reps=10):
+    """Per-row GB/s of the bandwidth-bound entry points on this workload (L2 flushed)."""
+    import diffusion_transformer_sequence_gb300 as usp
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    q = torch.randn(w.stack_shape, device="cuda").to(w.torch_dtype)
+    res = {}
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps + 2):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) * 1e-3)
+        return statistics.median(ts[2:])
+
+    X = usp.relayout_tok2head(q, w.ulysses, w.ring)
+    t = timed(lambda: usp.relayout_tok2head(q, w.ulysses, w.ring, out=X))
+    res["tok2head"] = {"GB/s": 2 * w.t_bytes / t / 1e9, "us": t * 1e6, "bytes": 2 * w.t_bytes}
+    T = torch.empty_like(q)
+    t = timed(lambda: usp.relayout_head2tok(X, w.ulysses, w.ring, out=T))
+    res["head2tok"] = {"GB/s": 2 * w.t_bytes / t / 1e9, "us": t * 1e6, "bytes": 2 * w.t_bytes}
+    if w.ring > 1:
+        R = w.ring
+        outs = torch.randn((R, w.B, w.H, w.N, w.D), device="cuda").to(w.torch_dtype)
+        lses = torch.randn((R, w.B, w.H, w.N), device="cuda")
+        o = torch.empty(outs.shape[1:], dtype=outs.dtype, device="cuda")
+        l = torch.empty(lses.shape[1:], device="cuda")
+        t = timed(lambda: usp.lse_merge(outs, lses, out=o, lse=l))
+        byt = (R + 1) * w.t_bytes + (R + 1) * w.B * w.H * w.N * 4
+        res["lse_merge"] = {"GB/s": byt / t / 1e9, "us": t * 1e6, "bytes": byt}
+    return res
+
+
+def our_arm(args, w, ws, rank, local):
+    torch.cuda.set_device(local)
+    import diffusion_transformer_sequence_gb300 as usp
+    usp.lib()
+    peaks = load_peaks()
+    step = Step(w, backward=False)
+    for _ in range(args.warmup):
+        step.flush()
+        step.run()
+    torch.cuda.synchronize()
+    if usp.device_status() != 0:
+        raise RuntimeError("device error status during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            step.flush()
+            step.run(evs[i])
+        torch.cuda.synchronize()
+    barrier(ws)
+    if usp.device_status() != 0:
+        raise RuntimeError("device error status during the timed steps")
+    mat = [e[0].elapsed_time(e[1]) * 1e-3 for e in evs]
+    fus = [e[1].elapsed_time(e[2]) * 1e-3 for e in evs]
+    step_s = sum(m + f for m, f in zip(mat, fus)) / args.steps
+    step_s = max_over_ranks(step_s, ws)
+    value = ws * step.flop() / step_s / 1e12
+
+    # end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        for _ in range(2):
+            step.run_e2e()
+        torch.cuda.synchronize()
+        barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            step.run_e2e()
+        b.record()
+        torch.cuda.synchronize()
+        e2e_s = max_over_ranks(a.elapsed_time(b) * 1e-3 / args.steps, ws)
+        h2d, d2h = step.io_bytes()
+        e2e = {"value": ws * step.flop() / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+
+    rows = time_rows(w) if rank == 0 else {}
+    if rank != 0:
+        return
+    fused_s = statistics.mean(fus)
+    mat_s = statistics.mean(mat)
+    fused_tflops = w.fwd_flop / fused_s / 1e12
+    peak = peaks["bf16_tflops"]
+    roofline = {"kernel": "attn_tc_fwd_kernel (fused USP forward, one launch)", "bound": "tensor",
+                "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s", "frac": fused_tflops / peak,
+                "traffic": None, "peak_kind": f"bf16 dense burst, {peaks['source']}"}
+    for k, r in rows.items():
+        r["frac_of_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
+    cpu = None
+    if not args.no_cpu_baseline:
+        heads = sample_heads(w)
+        dt = run_oracle_sample(w, heads)
+        cpu = {"value": oracle_sample_flop(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+               "kind": "oracle", "sample": f"oracle USP forward (numpy fp64) on {heads} of {w.H} heads, full N, "
+                                           f"{dt:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "desc": w.description, "global_batch": w.B * ws, "seq_len": w.N,
+                   "heads": w.H, "head_dim": w.D, "ulysses": w.ulysses, "ring": w.ring,
+                   "parallelism": f"{ws} independent replicas; u x r virtual ranks per device",
+                   "step": "usp_attention_fwd materialised + usp_attention_fwd fused",
+                   "l2": "flushed (256 MB write) before every timed step, outside the events"},
+        "rows": {"materialised_fwd_ms": mat_s * 1e3, "fused_fwd_ms": fused_s * 1e3,
+                 "materialised_fwd_tflops": w.fwd_flop / mat_s / 1e12, "fused_fwd_tflops": fused_tflops,
+                 **{k + "_GBps": v["GB/s"] for k, v in rows.items()},
+                 **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items()}},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": step.launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "peaks": peaks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
+    ap.add_argument("--workload", default="qwen1024", choices=wl.ORDER)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    ws, rank, local = dist_env()
+    w = wl.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        reference_arm(args, w, ws, rank)
+        return
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+    try:
+        our_arm(args, w, ws, rank, local)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

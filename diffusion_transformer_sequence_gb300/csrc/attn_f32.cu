@@ -1,0 +1,162 @@
+// fp32 attention with log-sum-exp on the FP32 pipes (no tensor cores: the
+// 1e-5 bound of the handbook's fp32 demo rules out tf32).
+//
+// One warp owns one query row.  The block stages K and V tiles of 32 keys in
+// shared memory; lane l scores key l of the tile, the row maximum and sum use
+// warp-shuffle reductions (online softmax), and each lane accumulates the
+// output dimensions d = lane + 32*i.  All arithmetic is IEEE fp32 with expf.
+//
+// Addressing modes:
+//  * plain / materialised: heads are contiguous [rows][D] blocks; a "unit"
+//    (one query head against one KV head) is mapped through the ring
+//    schedule: unit = (t, g, j, b, h') -> KV chunk c = (g - t) mod ring, and
+//    the output of ring step t goes to head t*out_step_stride + q_head.
+//  * fused: q/k/v/out are the token-sharded stack [sp][BH][Ns][D]; a unit is
+//    one (b, h) head attending over every shard's keys.
+#include "usp_internal.cuh"
+
+namespace usp {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kTileK = 32;
+
+struct F32Addr {
+  bool fused;
+  int64_t BH, Ns;  // fused: stack [sp][BH][Ns][D]
+  __device__ __forceinline__ int64_t row_off(int64_t head, int64_t row, int64_t nrows, int D) const {
+    if (!fused) return (head * nrows + row) * (int64_t)D;
+    const int64_t s = row / Ns, n = row - s * Ns;
+    return ((s * BH + head) * Ns + n) * (int64_t)D;
+  }
+  __device__ __forceinline__ int64_t lse_off(int64_t head, int64_t row, int64_t nrows) const {
+    if (!fused) return head * nrows + row;
+    const int64_t s = row / Ns, n = row - s * Ns;
+    return (s * BH + head) * Ns + n;
+  }
+};
+
+template <int kDmax>
+__global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    float* __restrict__ out, float* __restrict__ lse, int64_t Nq, int64_t Nk, int D, float scale,
+    RingSchedule sched, int64_t out_step_stride, F32Addr addr) {
+  __shared__ float Ks[kTileK][kDmax + 1];
+  __shared__ float Vs[kTileK][kDmax];
+  __shared__ float Qs[kWarps][kDmax];
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // unit -> (q head, kv head, out head)
+  const int64_t unit = blockIdx.y;
+  const int64_t per_step = (int64_t)sched.ring * sched.ulysses * sched.heads_per_rank;
+  const int64_t t = unit / per_step;
+  const int64_t qh = unit - t * per_step;
+  const int64_t rank_stride = (int64_t)sched.heads_per_rank;        // heads per virtual rank
+  const int64_t g = qh / (rank_stride * sched.ulysses);
+  const int64_t c = ((g - t) % sched.ring + sched.ring) % sched.ring;
+  const int64_t kvh = qh + (c - g) * rank_stride * sched.ulysses;
+  const int64_t oh = t * out_step_stride + qh;
+
+  const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+  const bool active = row < Nq;
+  if (active)
+    for (int d = lane; d < D; d += 32) Qs[warp][d] = q[addr.row_off(qh, row, Nq, D) + d];
+
+  float m = -INFINITY, l = 0.f;
+  float o[kDmax / 32];
+#pragma unroll
+  for (int i = 0; i < kDmax / 32; ++i) o[i] = 0.f;
+
+  for (int64_t j0 = 0; j0 < Nk; j0 += kTileK) {
+    __syncthreads();
+    const int nk = (int)((Nk - j0) < kTileK ? (Nk - j0) : kTileK);
+    for (int e = threadIdx.x; e < kTileK * D; e += blockDim.x) {
+      const int jj = e / D, d = e - jj * D;
+      float kv = 0.f, vv = 0.f;
+      if (jj < nk) {
+        const int64_t off = addr.row_off(kvh, j0 + jj, Nk, D) + d;
+        kv = k[off];
+        vv = v[off];
+      }
+      Ks[jj][d] = kv;
+      Vs[jj][d] = vv;
+    }
+    __syncthreads();
+    if (!active) continue;
+    float s = -INFINITY;
+    if (lane < nk) {
+      float acc = 0.f;
+      for (int d = 0; d < D; ++d) acc = fmaf(Qs[warp][d], Ks[lane][d], acc);
+      s = acc * scale;
+    }
+    float mx = s;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_new = fmaxf(m, mx);
+    const float p = (lane < nk) ? expf(s - m_new) : 0.f;
+    const float alpha = expf(m - m_new);  // m = -inf on the first tile -> 0
+    float ps = p;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l = l * alpha + ps;
+#pragma unroll
+    for (int i = 0; i < kDmax / 32; ++i) o[i] *= alpha;
+    for (int jj = 0; jj < nk; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+#pragma unroll
+      for (int i = 0; i < kDmax / 32; ++i) {
+        const int d = lane + 32 * i;
+        if (d < D) o[i] = fmaf(pj, Vs[jj][d], o[i]);
+      }
+    }
+    m = m_new;
+  }
+  if (!active) return;
+  const float inv = 1.f / l;
+  const int64_t ooff = addr.row_off(oh, row, Nq, D);
+#pragma unroll
+  for (int i = 0; i < kDmax / 32; ++i) {
+    const int d = lane + 32 * i;
+    if (d < D) out[ooff + d] = o[i] * inv;
+  }
+  if (lane == 0) lse[addr.lse_off(oh, row, Nq)] = m + logf(l);
+}
+
+template <int kDmax>
+cudaError_t launch_dmax(const float* q, const float* k, const float* v, float* out, float* lse,
+                        int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
+                        int64_t out_step_stride, F32Addr addr, int64_t units, cudaStream_t stream) {
+  dim3 grid((unsigned)((Nq + kWarps - 1) / kWarps), (unsigned)units, 1);
+  attn_f32_kernel<kDmax><<<grid, kWarps * 32, 0, stream>>>(q, k, v, out, lse, Nq, Nk, D, scale, sched,
+                                                           out_step_stride, addr);
+  return cudaGetLastError();
+}
+
+cudaError_t dispatch(const float* q, const float* k, const float* v, float* out, float* lse,
+                     int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
+                     int64_t out_step_stride, F32Addr addr, int64_t units, cudaStream_t stream) {
+  if (D <= 32) return launch_dmax<32>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
+  if (D <= 64) return launch_dmax<64>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
+  return launch_dmax<128>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* out, float* lse,
+                            int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
+                            int64_t out_step_stride_heads, cudaStream_t stream) {
+  const int64_t units = (int64_t)sched.steps * sched.ring * sched.ulysses * sched.heads_per_rank;
+  F32Addr addr{false, 0, 0};
+  return dispatch(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride_heads, addr, units, stream);
+}
+
+cudaError_t launch_attn_f32_fused(const float* q, const float* k, const float* v, float* out,
+                                  float* lse, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
+                                  cudaStream_t stream) {
+  RingSchedule sched{1, 1, 1, (int)BH};
+  F32Addr addr{true, BH, Ns};
+  const int64_t N = sp * Ns;
+  return dispatch(q, k, v, out, lse, N, N, D, scale, sched, 0, addr, BH, stream);
+}
+
+}  // namespace usp

@@ -1,0 +1,145 @@
+// The Ring step's log-sum-exp merge of R partial attention results.
+//
+// "Multi-GPU parallelism: spreading one step over several cards", section
+// "Sequence parallelism: Ulysses and Ring": each KV block that arrives round
+// the ring yields a local attention result, and the results are merged with a
+// log-sum-exp (the online-softmax formula).  Per row, in fp32:
+//   m = max_t lse_t;  L = m + ln sum_t exp(lse_t - m);  out = sum_t exp(lse_t - L) out_t
+// The merge is over the R ring steps of one row, not across D, so a row's D
+// elements are split over threads in 16-byte vectors and no cross-thread
+// reduction is needed.  HBM-bound: reads R rows of partials + R LSEs, writes
+// one row + one LSE.
+#include <cuda_bf16.h>
+
+#include "usp_internal.cuh"
+
+namespace usp {
+namespace {
+
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* f) {
+  uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float* f) {
+  uint4 raw;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = raw;
+}
+__device__ __forceinline__ void load8(const float* p, float* f) {
+  float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+__device__ __forceinline__ void store8(float* p, const float* f) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f(float* p, float x) { *p = x; }
+__device__ __forceinline__ void from_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Row statistics shared by both kernels: returns L, fills w[t] = exp(lse_t - L).
+template <int kMaxR>
+__device__ __forceinline__ float merge_weights(const float* __restrict__ lses, int R, int64_t rows,
+                                               int64_t row, float* w) {
+  float m = -INFINITY;
+  for (int t = 0; t < R; ++t) m = fmaxf(m, __ldg(lses + t * rows + row));
+  float s = 0.f;
+  for (int t = 0; t < R; ++t) s += expf(__ldg(lses + t * rows + row) - m);
+  const float L = m + logf(s);
+#pragma unroll
+  for (int t = 0; t < kMaxR; ++t)
+    if (t < R) w[t] = expf(__ldg(lses + t * rows + row) - L);
+  return L;
+}
+
+// 8 elements (16 or 32 bytes) per thread; D % 8 == 0, R <= kMaxR.
+template <typename T, int kMaxR>
+__global__ void __launch_bounds__(256) merge_vec_kernel(const T* __restrict__ outs,
+                                                        const float* __restrict__ lses, int R,
+                                                        T* __restrict__ out, float* __restrict__ lse,
+                                                        int64_t rows, int64_t D) {
+  const int64_t tpr = D / 8;
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = gt / tpr;
+  const int64_t c = (gt - row * tpr) * 8;
+  if (row >= rows) return;
+  float w[kMaxR];
+  const float L = merge_weights<kMaxR>(lses, R, rows, row, w);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  const int64_t plane = rows * D;
+#pragma unroll
+  for (int t = 0; t < kMaxR; ++t) {
+    if (t < R) {
+      float x[8];
+      load8(outs + t * plane + row * D + c, x);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[t], x[i], acc[i]);
+    }
+  }
+  store8(out + row * D + c, acc);
+  if (c == 0) lse[row] = L;
+}
+
+// Generic: one thread per output element (any D, any R).
+template <typename T>
+__global__ void __launch_bounds__(256) merge_scalar_kernel(const T* __restrict__ outs,
+                                                           const float* __restrict__ lses, int R,
+                                                           T* __restrict__ out, float* __restrict__ lse,
+                                                           int64_t rows, int64_t D) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= rows * D) return;
+  const int64_t row = gt / D;
+  float m = -INFINITY;
+  for (int t = 0; t < R; ++t) m = fmaxf(m, lses[t * rows + row]);
+  float s = 0.f;
+  for (int t = 0; t < R; ++t) s += expf(lses[t * rows + row] - m);
+  const float L = m + logf(s);
+  float acc = 0.f;
+  for (int t = 0; t < R; ++t) acc = fmaf(expf(lses[t * rows + row] - L), to_f(outs[t * rows * D + gt]), acc);
+  from_f(out + gt, acc);
+  if (gt - row * D == 0) lse[row] = L;
+}
+
+template <typename T>
+cudaError_t launch_typed(const void* outs, const float* lses, int R, void* out, float* lse, int64_t rows,
+                         int64_t D, cudaStream_t stream) {
+  const uintptr_t a = (uintptr_t)outs | (uintptr_t)out;
+  const bool vec = (D % 8 == 0) && ((a & 15) == 0) && R <= 8;
+  if (vec) {
+    const int64_t threads = rows * (D / 8);
+    const int64_t blocks = (threads + 255) / 256;
+    if (R <= 2)
+      merge_vec_kernel<T, 2><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
+    else if (R <= 4)
+      merge_vec_kernel<T, 4><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
+    else
+      merge_vec_kernel<T, 8><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
+  } else {
+    const int64_t blocks = (rows * D + 255) / 256;
+    merge_scalar_kernel<T><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
+                             int64_t rows, int64_t D, int dtype, cudaStream_t stream) {
+  if (dtype == 1) return launch_typed<__nv_bfloat16>(outs, lses, R, out, lse, rows, D, stream);
+  return launch_typed<float>(outs, lses, R, out, lse, rows, D, stream);
+}
+
+}  // namespace usp

@@ -1,0 +1,105 @@
+// Ulysses all-to-all as an on-device re-layout (token-sharded <-> head-sharded).
+//
+// Both directions are a batched copy of contiguous runs of Ns*D elements:
+//   tok2head: run (g, j, b, h', s) of the head-sharded stack
+//             X[g, j, b, h', s*Ns : (s+1)*Ns, :]  <-  T[g, s, b, j*Hu + h', :, :]
+//   head2tok: run (g, s, b, h) of the token-sharded stack
+//             T[g, s, b, h, :, :]  <-  X[g, h / Hu, b, h % Hu, s*Ns : (s+1)*Ns, :]
+// ("Multi-GPU parallelism: spreading one step over several cards", section
+// "Sequence parallelism: Ulysses and Ring": all_to_all_heads / _tokens.)
+// Every run is contiguous on both sides, so the kernel streams each run with
+// the widest aligned vector (16 bytes on every workload) and several loads in
+// flight per thread; staging through shared memory would add a copy without
+// improving coalescing.  Run-level index arithmetic happens once per CTA.
+#include "usp_internal.cuh"
+
+namespace usp {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+template <typename Vec>
+__device__ __forceinline__ Vec load_stream(const Vec* p) { return __ldg(p); }
+
+template <typename Vec, bool kTok2Head>
+__global__ void __launch_bounds__(kThreads) relayout_kernel(const Vec* __restrict__ src,
+                                                            Vec* __restrict__ dst, int64_t nruns,
+                                                            int64_t run_vecs, int64_t B, int64_t H,
+                                                            int64_t Hu, int64_t u) {
+  for (int64_t run = blockIdx.y; run < nruns; run += gridDim.y) {
+    int64_t src_run;
+    if (kTok2Head) {
+      // destination run order (g, j, b, h', s)
+      int64_t t = run;
+      const int64_t s = t % u; t /= u;
+      const int64_t hp = t % Hu; t /= Hu;
+      const int64_t b = t % B; t /= B;
+      const int64_t j = t % u;
+      const int64_t g = t / u;
+      src_run = ((g * u + s) * B + b) * H + j * Hu + hp;
+    } else {
+      // destination run order (g, s, b, h)
+      int64_t t = run;
+      const int64_t h = t % H; t /= H;
+      const int64_t b = t % B; t /= B;
+      const int64_t s = t % u;
+      const int64_t g = t / u;
+      const int64_t j = h / Hu, hp = h % Hu;
+      src_run = (((g * u + j) * B + b) * Hu + hp) * u + s;
+    }
+    const Vec* __restrict__ sp = src + src_run * run_vecs;
+    Vec* __restrict__ dp = dst + run * run_vecs;
+    const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
+    for (int64_t i0 = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; i0 < run_vecs; i0 += step) {
+      Vec tmp[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const int64_t i = i0 + (int64_t)k * kThreads;
+        if (i < run_vecs) tmp[k] = load_stream(sp + i);
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        const int64_t i = i0 + (int64_t)k * kThreads;
+        if (i < run_vecs) dp[i] = tmp[k];
+      }
+    }
+  }
+}
+
+template <typename Vec>
+cudaError_t launch_vec(const void* src, void* dst, int64_t nruns, int64_t run_bytes, int64_t B,
+                       int64_t H, int64_t Hu, int64_t u, bool tok2head, cudaStream_t stream) {
+  const int64_t run_vecs = run_bytes / (int64_t)sizeof(Vec);
+  const int64_t per_cta = (int64_t)kThreads * kUnroll;
+  int64_t gx = (run_vecs + per_cta - 1) / per_cta;
+  if (gx > 1024) gx = 1024;
+  int64_t gy = nruns < 65535 ? nruns : 65535;
+  dim3 grid((unsigned)gx, (unsigned)gy, 1);
+  if (tok2head)
+    relayout_kernel<Vec, true><<<grid, kThreads, 0, stream>>>((const Vec*)src, (Vec*)dst, nruns,
+                                                             run_vecs, B, H, Hu, u);
+  else
+    relayout_kernel<Vec, false><<<grid, kThreads, 0, stream>>>((const Vec*)src, (Vec*)dst, nruns,
+                                                              run_vecs, B, H, Hu, u);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_relayout(const void* src, void* dst, int64_t /*runs_outer*/, int64_t B, int64_t H,
+                            int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
+                            cudaStream_t stream) {
+  const int64_t u = ulysses;
+  const int64_t Hu = H / u;
+  const int64_t nruns = (int64_t)ring * u * B * H;
+  const int64_t run_bytes = Ns * D * elt;
+  const uintptr_t a = (uintptr_t)src | (uintptr_t)dst | (uintptr_t)run_bytes;
+  if ((a & 15) == 0) return launch_vec<uint4>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  if ((a & 7) == 0) return launch_vec<uint2>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  if ((a & 3) == 0) return launch_vec<uint32_t>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  if ((a & 1) == 0) return launch_vec<uint16_t>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  return launch_vec<uint8_t>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+}
+
+}  // namespace usp

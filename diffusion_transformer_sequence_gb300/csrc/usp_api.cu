@@ -1,0 +1,329 @@
+// libusp C ABI: argument validation, workspace layout and the USP drivers.
+//
+// The driver composes the steps of USP attention as the USP PR page's Design
+// describes usp_attention (Ulysses all-to-all, Ring steps with an
+// LSE-returning kernel, all-to-all back), with the virtual rank grid
+// ulysses x ring laid out on one device:
+//   * the all-to-all becomes the on-device re-layout (relayout.cu);
+//   * the ring's peer-to-peer KV rotation becomes addressing: at ring step t
+//     rank g reads KV chunk (g - t) mod ring in place, nothing is copied;
+//   * the per-step results are merged by log-sum-exp (lse_merge.cu).
+// Validation mirrors the PR page's Limitations table: every unsupported
+// configuration fails loudly, before anything is enqueued.
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "../../include/usp.h"
+#include "usp_internal.cuh"
+
+namespace usp {
+
+__device__ unsigned int g_dev_error = 0;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<long long> g_spin_limit{-1};
+constexpr long long kDefaultSpinLimit = 1LL << 40;       // polls; the time bound below governs
+constexpr unsigned long long kWaitNs = 2000000000ull;    // 2 s per wait
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return USP_ERR_CUDA;
+}
+
+int err_word(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return USP_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dev_error);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_err_ptr[dev];
+  return USP_OK;
+}
+
+int guard(Guard* g) {
+  unsigned int* p = nullptr;
+  int st = err_word(&p);
+  if (st != USP_OK) return st;
+  long long lim = g_spin_limit.load();
+  g->err = p;
+  g->spin_limit = lim < 0 ? kDefaultSpinLimit : lim;
+  g->ns_limit = kWaitNs;
+  return USP_OK;
+}
+
+size_t elt_size(usp_dtype d) { return d == USP_BF16 ? 2 : 4; }
+bool dtype_ok(usp_dtype d) { return d == USP_F32 || d == USP_BF16; }
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_dims(int64_t B, int64_t H, int64_t N, int64_t D, int u, int r) {
+  if (B < 0 || H < 0 || N < 0 || D < 1 || u < 1 || r < 1) return USP_ERR_INVALID_ARG;
+  if (H % u != 0) return USP_ERR_DIVISIBILITY;               // Ulysses degree must divide the heads
+  if (N % ((int64_t)u * r) != 0) return USP_ERR_DIVISIBILITY;  // no padding: N % sp == 0
+  return USP_OK;
+}
+
+// Kernel support for a (dtype, D) pair.
+int check_kernel(usp_dtype dt, int64_t D) {
+  if (!dtype_ok(dt)) return USP_ERR_UNSUPPORTED;
+  if (dt == USP_BF16 && D != 128) return USP_ERR_UNSUPPORTED;
+  if (dt == USP_F32 && D > 128) return USP_ERR_UNSUPPORTED;
+  return USP_OK;
+}
+
+struct FwdWorkspace {
+  size_t xq, xk, xv, parts_o, parts_l, xo, xl, total;
+};
+FwdWorkspace fwd_layout(int64_t B, int64_t H, int64_t N, int64_t D, int r, usp_dtype dt) {
+  const size_t t = round_up((size_t)(B * H * N * D) * elt_size(dt));
+  const size_t lb = round_up((size_t)(B * H * N) * 4);
+  FwdWorkspace w{};
+  size_t off = 0;
+  w.xq = off; off += t;
+  w.xk = off; off += t;
+  w.xv = off; off += t;
+  if (r > 1) {
+    w.parts_o = off; off += (size_t)r * t;
+    w.parts_l = off; off += (size_t)r * lb;
+  }
+  w.xo = off; off += t;
+  w.xl = off; off += lb;
+  w.total = off;
+  return w;
+}
+
+int relayout(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_t D, int u, int r,
+             int elt, bool tok2head, cudaStream_t s) {
+  const int64_t Ns = N / ((int64_t)u * r);
+  cudaError_t e = launch_relayout(src, dst, 0, B, H, Ns, D, u, r, elt, tok2head, s);
+  return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+
+// Per-(rank, ring step) chunk attention over the head-sharded stacks.
+int chunk_attention(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B,
+                    int64_t Hu, int64_t Nr, int64_t D, int u, int r, float scale, usp_dtype dt,
+                    cudaStream_t s) {
+  RingSchedule sched{u, r, r, (int)(B * Hu)};
+  const int64_t step_heads = (int64_t)r * u * B * Hu;
+  cudaError_t e;
+  if (dt == USP_F32) {
+    e = launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)out, lse, Nr, Nr, (int)D,
+                        scale, sched, step_heads, s);
+  } else {
+    Guard g;
+    int st = guard(&g);
+    if (st != USP_OK) return st;
+    TcAttnArgs a{};
+    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+    a.Nq = Nr; a.Nk = Nr;
+    a.sched = sched;
+    a.out_step_stride_heads = step_heads;
+    a.fused = false;
+    a.scale = scale;
+    e = launch_attn_tc_fwd(a, g, s);
+  }
+  return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+
+}  // namespace
+}  // namespace usp
+
+using namespace usp;
+
+extern "C" {
+
+int usp_relayout_tok2head(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_t D, int ulysses,
+                          int ring, usp_dtype dtype, usp_stream_t stream) {
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  if (!dtype_ok(dtype)) return USP_ERR_UNSUPPORTED;
+  if (B * H * N == 0) return USP_OK;
+  if (!src || !dst) return USP_ERR_INVALID_ARG;
+  return relayout(src, dst, B, H, N, D, ulysses, ring, (int)elt_size(dtype), true, (cudaStream_t)stream);
+}
+
+int usp_relayout_head2tok(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_t D, int ulysses,
+                          int ring, usp_dtype dtype, usp_stream_t stream) {
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  if (!dtype_ok(dtype)) return USP_ERR_UNSUPPORTED;
+  if (B * H * N == 0) return USP_OK;
+  if (!src || !dst) return USP_ERR_INVALID_ARG;
+  return relayout(src, dst, B, H, N, D, ulysses, ring, (int)elt_size(dtype), false, (cudaStream_t)stream);
+}
+
+int usp_attn_chunk_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B, int64_t H,
+                       int64_t Nq, int64_t Nk, int64_t D, float scale, usp_dtype dtype, usp_stream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || D < 1) return USP_ERR_INVALID_ARG;
+  if (Nk < 1) return USP_ERR_INVALID_ARG;  // softmax over an empty key set is undefined
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  int st = check_kernel(dtype, D);
+  if (st != USP_OK) return st;
+  if (B * H * Nq == 0) return USP_OK;
+  if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
+  if (B * H > 65535) return USP_ERR_UNSUPPORTED;
+  if (dtype == USP_BF16 && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16)))
+    return USP_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return USP_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  RingSchedule sched{1, 1, 1, (int)(B * H)};
+  cudaError_t e;
+  if (dtype == USP_F32) {
+    e = launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)out, lse, Nq, Nk, (int)D,
+                        scale, sched, 0, s);
+  } else {
+    Guard g;
+    st = guard(&g);
+    if (st != USP_OK) return st;
+    TcAttnArgs a{};
+    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+    a.Nq = Nq; a.Nk = Nk;
+    a.sched = sched;
+    a.out_step_stride_heads = 0;
+    a.fused = false;
+    a.scale = scale;
+    e = launch_attn_tc_fwd(a, g, s);
+  }
+  return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+
+int usp_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse, int64_t B, int64_t H,
+                  int64_t Nq, int64_t D, usp_dtype dtype, usp_stream_t stream) {
+  if (B < 0 || H < 0 || Nq < 0 || D < 1 || R < 1) return USP_ERR_INVALID_ARG;
+  if (!dtype_ok(dtype)) return USP_ERR_UNSUPPORTED;
+  if (B * H * Nq == 0) return USP_OK;
+  if (!outs || !lses || !out || !lse) return USP_ERR_INVALID_ARG;
+  cudaError_t e = launch_lse_merge(outs, lses, R, out, lse, B * H * Nq, D, (int)dtype, (cudaStream_t)stream);
+  return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+
+size_t usp_attention_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring,
+                                     usp_dtype dtype, usp_mode mode, int backward) {
+  if (check_dims(B, H, N, D, ulysses, ring) != USP_OK || check_kernel(dtype, D) != USP_OK) return 0;
+  if (backward) return 0;
+  if (mode == USP_FUSED) return 0;
+  return fwd_layout(B, H, N, D, ring, dtype).total;
+}
+
+int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B, int64_t H,
+                      int64_t N, int64_t D, int ulysses, int ring, float scale, usp_dtype dtype, usp_mode mode,
+                      void* workspace, size_t workspace_bytes, usp_stream_t stream) {
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  if (mode != USP_MATERIALISED && mode != USP_FUSED) return USP_ERR_INVALID_ARG;
+  st = check_kernel(dtype, D);
+  if (st != USP_OK) return st;
+  if (B * H * N == 0) return USP_OK;
+  if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
+  if (dtype == USP_BF16 && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16)))
+    return USP_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return USP_ERR_INVALID_ARG;
+  const int u = ulysses, r = ring;
+  const int64_t sp = (int64_t)u * r, Ns = N / sp, Nr = N / r, Hu = H / u;
+  cudaStream_t s = (cudaStream_t)stream;
+
+  if (mode == USP_FUSED) {
+    if (B * H > 65535) return USP_ERR_UNSUPPORTED;
+    cudaError_t e;
+    if (dtype == USP_F32) {
+      e = launch_attn_f32_fused((const float*)q, (const float*)k, (const float*)v, (float*)out, lse, B * H, sp,
+                                Ns, (int)D, scale, s);
+    } else {
+      Guard g;
+      st = guard(&g);
+      if (st != USP_OK) return st;
+      TcAttnArgs a{};
+      a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+      a.fused = true;
+      a.BH = B * H; a.sp = sp; a.Ns = Ns;
+      a.scale = scale;
+      e = launch_attn_tc_fwd(a, g, s);
+    }
+    return e == cudaSuccess ? USP_OK : cuda_fail(e);
+  }
+
+  // materialised
+  if ((int64_t)r * r * u * B * Hu > 65535) return USP_ERR_UNSUPPORTED;
+  const FwdWorkspace w = fwd_layout(B, H, N, D, r, dtype);
+  if (!workspace || workspace_bytes < w.total) return USP_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return USP_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  const int elt = (int)elt_size(dtype);
+  if ((st = relayout(q, ws + w.xq, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
+  if ((st = relayout(k, ws + w.xk, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
+  if ((st = relayout(v, ws + w.xv, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
+  void* o_dst = r > 1 ? (void*)(ws + w.parts_o) : (void*)(ws + w.xo);
+  float* l_dst = r > 1 ? (float*)(ws + w.parts_l) : (float*)(ws + w.xl);
+  if ((st = chunk_attention(ws + w.xq, ws + w.xk, ws + w.xv, o_dst, l_dst, B, Hu, Nr, D, u, r, scale, dtype, s)) !=
+      USP_OK)
+    return st;
+  if (r > 1) {
+    cudaError_t e = launch_lse_merge(ws + w.parts_o, (const float*)(ws + w.parts_l), r, ws + w.xo,
+                                     (float*)(ws + w.xl), B * H * N, D, (int)dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if ((st = relayout(ws + w.xo, out, B, H, N, D, u, r, elt, false, s)) != USP_OK) return st;
+  return relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s);
+}
+
+int usp_attention_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N, int64_t D,
+                      int ulysses, int ring, float scale, usp_dtype dtype, void* workspace, size_t workspace_bytes,
+                      usp_stream_t stream) {
+  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
+  (void)workspace; (void)workspace_bytes; (void)stream; (void)scale;
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  return USP_ERR_UNSUPPORTED;
+}
+
+int usp_device_status(usp_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned int* p = nullptr;
+  int st = err_word(&p);
+  if (st != USP_OK) return st;
+  unsigned int v = 0;
+  e = cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (v != 0) {
+    const unsigned int zero = 0;
+    e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return USP_ERR_TIMEOUT;
+  }
+  return USP_OK;
+}
+
+const char* usp_status_string(int status) {
+  switch (status) {
+    case USP_OK: return "USP_OK";
+    case USP_ERR_INVALID_ARG: return "USP_ERR_INVALID_ARG";
+    case USP_ERR_DIVISIBILITY: return "USP_ERR_DIVISIBILITY";
+    case USP_ERR_UNSUPPORTED: return "USP_ERR_UNSUPPORTED";
+    case USP_ERR_WORKSPACE: return "USP_ERR_WORKSPACE";
+    case USP_ERR_CUDA: return "USP_ERR_CUDA";
+    case USP_ERR_TIMEOUT: return "USP_ERR_TIMEOUT";
+    default: return "USP_ERR_UNKNOWN";
+  }
+}
+
+int usp_last_cuda_error(void) { return t_last_cuda_error; }
+
+void usp_set_spin_limit(long long polls) { g_spin_limit.store(polls < 0 ? -1 : polls); }
+
+}  // extern "C"

@@ -1,0 +1,179 @@
+/*
+ * usp.h -- C ABI of libusp: the attention step of a diffusion transformer
+ * under USP (Ulysses x Ring) sequence parallelism, with the rank grid of
+ * ulysses x ring virtual ranks simulated on ONE GPU (GB300, sm_103a).
+ *
+ * Sources (web pages, by title):
+ *  [HB] "Multi-GPU parallelism: spreading one step over several cards",
+ *       section "Sequence parallelism: Ulysses and Ring": the Ulysses
+ *       all-to-all (per-card token slices <-> per-card head groups), per-card
+ *       attention, and the Ring step that merges per-KV-block results with a
+ *       log-sum-exp (FlashAttention's online-softmax formula).
+ *  [PR] "Feat: USP sequence parallelism (Ulysses x Ring) via
+ *       SequenceParallelPlan; Wan enabled": Design ("Coordinates": sp =
+ *       ulysses x ring, Ulysses ranks contiguous, ring ranks strided; "Ring
+ *       kernel selection": kernels return LSE and pair with a real backward),
+ *       Limitations (the conditions that must fail loudly), Numerics.
+ *  [VO] vllm-omni "Parallelism Acceleration Guide": sequence chunked by SP
+ *       rank in rank order; hybrid sp = ulysses_degree x ring_degree.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  * All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    owned by the caller; the library never allocates, frees or retains
+ *    them.  Buffers that a call writes must not overlap buffers it reads.
+ *  * Every call is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream) and returns after enqueueing its kernels.
+ *  * Arguments are validated on the host BEFORE anything is enqueued; an
+ *    invalid call enqueues nothing and returns a USP_ERR_* code.  An empty
+ *    problem (a zero B, H or row count where allowed) enqueues nothing and
+ *    returns USP_OK.
+ *  * Pointers handed to the tensor-core (bf16) paths must be 16-byte
+ *    aligned (tensor-memory-accelerator copies); misaligned pointers return
+ *    USP_ERR_INVALID_ARG.
+ *  * Device-side waits are bounded.  If one expires the kernel records it in
+ *    a per-device error word and returns early (outputs are then undefined);
+ *    usp_device_status() reports it.  No kernel traps or asserts.
+ *  * Layouts (row-major, innermost last):
+ *      plain           [B, H, N, D]
+ *      token-sharded   [ring, ulysses, B, H, Ns, D], Ns = N/(ulysses*ring):
+ *                      virtual rank (g, j) -- ring index g, Ulysses index j,
+ *                      sp_rank = g*ulysses + j -- holds tokens
+ *                      [sp_rank*Ns, (sp_rank+1)*Ns) of every head ([PR]
+ *                      Coordinates; [VO] chunk by rank).  With
+ *                      ulysses = ring = 1 this is the plain layout.
+ *      head-sharded    [ring, ulysses, B, H/ulysses, Nr, D], Nr = N/ring:
+ *                      rank (g, j) holds heads [j*Hu, (j+1)*Hu) of the
+ *                      tokens of ring group g, source ranks concatenated in
+ *                      rank order ([HB] all_to_all_heads).
+ *      LSE             one fp32 per (row, head): the layouts above without
+ *                      the trailing D; natural logarithm.
+ */
+#ifndef USP_H
+#define USP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* usp_stream_t; /* a cudaStream_t */
+
+typedef enum { USP_F32 = 0, USP_BF16 = 1 } usp_dtype;
+
+typedef enum {
+  USP_MATERIALISED = 0, /* re-layout, per-(rank, ring step) attention, merge, re-layout back */
+  USP_FUSED = 1         /* one kernel reading and writing the token-sharded stacks in place */
+} usp_mode;
+
+enum {
+  USP_OK = 0,
+  USP_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer, scale not finite */
+  USP_ERR_DIVISIBILITY = 2, /* H % ulysses != 0 or N % (ulysses*ring) != 0 ([PR] Limitations) */
+  USP_ERR_UNSUPPORTED = 3,  /* dtype / head dim combination without a kernel */
+  USP_ERR_WORKSPACE = 4,    /* workspace null or smaller than usp_attention_workspace_bytes() */
+  USP_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed; see usp_last_cuda_error() */
+  USP_ERR_TIMEOUT = 6       /* a bounded device-side wait expired (usp_device_status) */
+};
+
+/* Ulysses all-to-all, token -> head, as an on-device re-layout ([HB]
+ * all_to_all_heads; [PR] Design, usp_attention's first step).
+ *   dst[g, j, b, h', s*Ns + n, d] = src[g, s, b, j*Hu + h', n, d]
+ * src: token-sharded stack [ring, ulysses, B, H, Ns, D]; dst: head-sharded
+ * stack [ring, ulysses, B, Hu, Nr, D].  Pure indexing, bit-exact, any
+ * element type of `dtype`'s width; for the LSE pass USP_F32 with D = 1.
+ * Errors: INVALID_ARG (null, negative size, ulysses/ring < 1),
+ * DIVISIBILITY (H % ulysses, N % (ulysses*ring)), CUDA. */
+int usp_relayout_tok2head(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_t D,
+                          int ulysses, int ring, usp_dtype dtype, usp_stream_t stream);
+
+/* The inverse re-layout, head -> token ([HB] all_to_all_tokens).
+ *   dst[g, s, b, j*Hu + h', n, d] = src[g, j, b, h', s*Ns + n, d]
+ * Same arguments, errors and layouts with src and dst exchanged. */
+int usp_relayout_head2tok(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_t D,
+                          int ulysses, int ring, usp_dtype dtype, usp_stream_t stream);
+
+/* Attention of one (query block, KV chunk) pair, returning the output and
+ * the log-sum-exp ([HB] per-card attention; [PR] "Ring kernel selection":
+ * kernels return LSE).  For every (b, h) and query row i:
+ *   S_ij = scale * q_i . k_j,  lse_i = ln sum_j exp(S_ij),
+ *   out_i = sum_j exp(S_ij - lse_i) v_j.
+ * No mask, not causal, no dropout.  q, out: [B, H, Nq, D]; k, v:
+ * [B, H, Nk, D], all in `dtype`; lse: [B, H, Nq] fp32.  bf16 runs on the
+ * tcgen05 tensor cores with fp32 accumulation (D = 128); fp32 runs on the
+ * FP32 pipes in full fp32 (D <= 128).
+ * Errors: INVALID_ARG (null, Nk < 1, negative size, non-finite scale,
+ * misaligned), UNSUPPORTED (head dim), CUDA. */
+int usp_attn_chunk_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                       usp_dtype dtype, usp_stream_t stream);
+
+/* The Ring step's log-sum-exp merge of R partial results over disjoint KV
+ * chunks ([HB] Ring paragraph; the formula is the standard one):
+ *   m = max_t lse_t,  lse = m + ln sum_t exp(lse_t - m),
+ *   out = sum_t exp(lse_t - lse) * out_t
+ * outs: R contiguous [B, H, Nq, D] blocks in `dtype`; lses: R contiguous
+ * [B, H, Nq] fp32 blocks; out: [B, H, Nq, D] `dtype`; lse: [B, H, Nq] fp32.
+ * Arithmetic in fp32.  Errors: INVALID_ARG (null, R < 1), CUDA. */
+int usp_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
+                  int64_t B, int64_t H, int64_t Nq, int64_t D, usp_dtype dtype, usp_stream_t stream);
+
+/* Bytes of workspace usp_attention_fwd (backward = 0) or usp_attention_bwd
+ * (backward = 1) needs for this problem; 0 when none is needed.  Returns 0
+ * as well for arguments the call itself would reject. */
+size_t usp_attention_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring,
+                                     usp_dtype dtype, usp_mode mode, int backward);
+
+/* USP attention forward over `ulysses` x `ring` virtual ranks ([PR] Design:
+ * Ulysses all-to-all, then the Ring steps with an LSE-returning kernel, then
+ * the all-to-all back).  q, k, v, out: token-sharded stacks
+ * [ring, ulysses, B, H, Ns, D]; lse: [ring, ulysses, B, H, Ns] fp32.
+ * The result equals unsharded attention of the re-assembled sequence.
+ *   USP_MATERIALISED: tok2head(q,k,v) -> for every rank (g, j) and ring step
+ *     t the chunk attention against KV chunk (g - t) mod ring -> merge over
+ *     t -> head2tok(out, lse).  Partial outputs are stored in `dtype`.
+ *     Needs usp_attention_workspace_bytes() of workspace.
+ *   USP_FUSED: one kernel reads q, k, v in place and keeps the ring merge
+ *     in registers (online softmax over every KV chunk); no workspace.
+ * Errors: INVALID_ARG, DIVISIBILITY, UNSUPPORTED, WORKSPACE, CUDA. */
+int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+                      int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring, float scale,
+                      usp_dtype dtype, usp_mode mode, void* workspace, size_t workspace_bytes,
+                      usp_stream_t stream);
+
+/* USP attention backward ([PR] Numerics: the all-to-all is a permutation so
+ * gradients flow through its inverse; each ring step uses its own KV chunk
+ * and the MERGED lse).  With P = exp(scale q k^T - lse):
+ *   dV = P^T dO, dP = dO V^T, Delta_i = sum_d dO_id O_id,
+ *   dS = P * (dP - Delta), dQ = scale dS K, dK = scale dS^T Q.
+ * q, k, v, out, dout, dq, dk, dv: token-sharded stacks in `dtype`; lse: the
+ * forward's fp32 LSE.  Needs usp_attention_workspace_bytes(..., 1).
+ * Errors: as usp_attention_fwd. */
+int usp_attention_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                      const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
+                      int64_t D, int ulysses, int ring, float scale, usp_dtype dtype, void* workspace,
+                      size_t workspace_bytes, usp_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns USP_OK, USP_ERR_TIMEOUT if a bounded device wait expired
+ * since the last call, or USP_ERR_CUDA. */
+int usp_device_status(usp_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* usp_status_string(int status);
+
+/* The cudaError_t of the last USP_ERR_CUDA return on this thread (0 if none). */
+int usp_last_cuda_error(void);
+
+/* Test hook: the number of polls a device-side wait may make before it
+ * gives up (negative restores the default).  0 makes every wait that is not
+ * already satisfied expire, so the timeout path runs without any hang. */
+void usp_set_spin_limit(long long polls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USP_H */

@@ -1,0 +1,112 @@
+"""C-ABI boundary tests that need no GPU: the library builds and loads, exports
+every symbol include/usp.h declares, and rejects invalid arguments on the host
+before touching CUDA (the USP PR page's Limitations: every configuration
+outside the supported envelope fails loudly)."""
+import ctypes
+
+import pytest
+
+from tests.helpers import ensure_built
+
+
+@pytest.fixture(scope="module")
+def L():
+    ensure_built()
+    from diffusion_transformer_sequence_gb300 import _lib
+    return _lib.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    from diffusion_transformer_sequence_gb300 import _lib
+    declared = _lib.header_symbols()
+    assert len(declared) >= 11
+    handle = ctypes.CDLL(_lib.LIB_PATH)
+    for name in declared:
+        assert hasattr(handle, name), f"libusp.so does not export {name}"
+    assert set(declared) == set(_lib.SIGNATURES), "binding signatures out of sync with usp.h"
+
+
+def test_status_strings(L):
+    from diffusion_transformer_sequence_gb300 import _lib
+    for code, name in [(0, "USP_OK"), (1, "USP_ERR_INVALID_ARG"), (2, "USP_ERR_DIVISIBILITY"),
+                       (3, "USP_ERR_UNSUPPORTED"), (4, "USP_ERR_WORKSPACE"), (5, "USP_ERR_CUDA"),
+                       (6, "USP_ERR_TIMEOUT")]:
+        assert L.usp_status_string(code).decode() == name
+    assert L.usp_last_cuda_error() == 0
+
+
+FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
+
+
+@pytest.mark.parametrize("fn", ["usp_relayout_tok2head", "usp_relayout_head2tok"])
+def test_relayout_validation(L, fn):
+    f = getattr(L, fn)
+    assert f(FAKE, FAKE, 1, 6, 256, 32, 4, 1, 0, None) == 2      # H % ulysses
+    assert f(FAKE, FAKE, 1, 8, 250, 32, 4, 1, 0, None) == 2      # N % sp
+    assert f(FAKE, FAKE, 1, 8, 256, 32, 2, 3, 0, None) == 2      # N % (u*r)
+    assert f(FAKE, FAKE, 1, 8, 256, 32, 0, 1, 0, None) == 1      # ulysses < 1
+    assert f(FAKE, FAKE, 1, 8, 256, 32, 1, 0, 0, None) == 1      # ring < 1
+    assert f(FAKE, FAKE, -1, 8, 256, 32, 1, 1, 0, None) == 1     # negative size
+    assert f(FAKE, FAKE, 1, 8, 256, 0, 1, 1, 0, None) == 1       # D < 1
+    assert f(None, FAKE, 1, 8, 256, 32, 4, 1, 0, None) == 1      # null src
+    assert f(FAKE, None, 1, 8, 256, 32, 4, 1, 0, None) == 1      # null dst
+    assert f(FAKE, FAKE, 1, 8, 256, 32, 4, 1, 7, None) == 3      # unknown dtype
+    assert f(None, None, 0, 8, 256, 32, 4, 1, 0, None) == 0      # empty problem: no-op
+    assert f(None, None, 1, 8, 0, 32, 4, 1, 0, None) == 0
+
+
+def test_chunk_validation(L):
+    f = L.usp_attn_chunk_fwd
+    a = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert f(*a, 1, 2, 256, 0, 128, 0.1, 1, None) == 1           # no keys
+    assert f(*a, 1, 2, 256, 256, 64, 0.1, 1, None) == 3          # bf16 needs D = 128
+    assert f(*a, 1, 2, 256, 256, 256, 0.1, 0, None) == 3         # fp32 D > 128
+    assert f(*a, 1, 2, 256, 256, 128, float("nan"), 1, None) == 1
+    assert f(*a, 1, 2, 256, 256, 128, float("inf"), 1, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, None, 1, 2, 256, 256, 128, 0.1, 1, None) == 1
+    assert f(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, 0.1, 1, None) == 1  # misaligned for TMA
+    assert f(None, None, None, None, None, 1, 2, 0, 256, 128, 0.1, 1, None) == 0     # no queries: no-op
+
+
+def test_merge_validation(L):
+    f = L.usp_lse_merge
+    assert f(FAKE, FAKE, 0, FAKE, FAKE, 1, 2, 8, 128, 1, None) == 1   # R < 1
+    assert f(None, FAKE, 2, FAKE, FAKE, 1, 2, 8, 128, 1, None) == 1
+    assert f(FAKE, FAKE, 2, FAKE, FAKE, 1, 2, 8, 128, 9, None) == 3
+    assert f(None, None, 2, None, None, 1, 2, 0, 128, 1, None) == 0
+
+
+def test_attention_validation_and_workspace(L):
+    f = L.usp_attention_fwd
+    a = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert f(*a, 1, 40, 32768, 128, 16, 1, 0.1, 1, 0, None, 0, None) == 2   # ulysses > H (40 % 16)
+    assert f(*a, 1, 40, 32770, 128, 8, 4, 0.1, 1, 0, None, 0, None) == 2    # N % sp
+    assert f(*a, 1, 40, 32768, 128, 8, 4, 0.1, 1, 5, None, 0, None) == 1    # bad mode
+    assert f(*a, 1, 40, 32768, 64, 8, 4, 0.1, 1, 0, None, 0, None) == 3     # bf16 D != 128
+    assert f(*a, 1, 40, 32768, 128, 8, 4, 0.1, 1, 0, None, 0, None) == 4    # no workspace
+    ws = L.usp_attention_workspace_bytes(1, 40, 32768, 128, 8, 4, 1, 0, 0)
+    t = 40 * 32768 * 128 * 2
+    lb = 40 * 32768 * 4
+    assert ws == 3 * t + 4 * t + 4 * lb + t + lb
+    assert f(*a, 1, 40, 32768, 128, 8, 4, 0.1, 1, 0, FAKE, ws - 1, None) == 4
+    assert L.usp_attention_workspace_bytes(1, 40, 32768, 128, 8, 4, 1, 1, 0) == 0   # fused: none
+    assert L.usp_attention_workspace_bytes(1, 24, 16384, 128, 4, 1, 1, 0, 0) == 4 * 24 * 16384 * 128 * 2 + 24 * 16384 * 4
+    assert L.usp_attention_workspace_bytes(1, 6, 256, 128, 4, 1, 1, 0, 0) == 0      # invalid -> 0
+    assert f(None, None, None, None, None, 1, 8, 0, 32, 4, 1, 0.1, 0, 1, None, 0, None) == 0  # empty
+
+
+def test_product_path_does_not_import_oracle():
+    import subprocess
+    import sys
+    code = ("import sys, diffusion_transformer_sequence_gb300 as u; u.lib(); "
+            "import diffusion_transformer_sequence_gb300.api, diffusion_transformer_sequence_gb300.workloads; "
+            "assert not any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules), sorted(sys.modules)")
+    subprocess.run([sys.executable, "-c", code], check=True)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    from diffusion_transformer_sequence_gb300 import _lib
+    monkeypatch.setattr(_lib, "_LIB", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "libusp.so"))
+    with pytest.raises(RuntimeError, match="no fallback"):
+        _lib.lib()
