@@ -64,7 +64,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except (OSError, FileNotFoundError):
@@ -73,7 +73,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -84,9 +87,14 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        t0, t1 = getattr(self, "start", 0.0), getattr(self, "end", float("inf"))
+        window = [ln for (t, ln) in self.lines if t0 <= t <= t1 + 0.05]
+        in_window = len(window)
+        if not window:  # timed region shorter than the sampling period: use the whole run
+            window = [ln for (_, ln) in self.lines]
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in window:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -99,7 +107,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "samples_in_timed_region": in_window}
 
 
 def dist_env():
@@ -146,22 +154,45 @@ def cpu_cores():
 
 
 def sample_heads(w):
-    # smallest head count the Ulysses split allows, enough for ~10-30 s of CPU work
-    return min(w.H, max(w.ulysses, (w.H // 2) // w.ulysses * w.ulysses))
+    """Heads of the workload the CPU-baseline leg runs (a multiple of ulysses):
+    the whole workload when it is small, else about a quarter of its heads."""
+    if w.fwd_flop <= 0.25e12:
+        return w.H
+    return min(w.H, max(w.ulysses, (w.H // 4) // w.ulysses * w.ulysses))
 
 
 def reference_arm(args, w, ws, rank):
+    """The oracle, as it stands, timed on the host cores (rank 0 only).
+
+    Each step is a bounded sample of the workload: the oracle's attention of
+    `rows` query rows of one head against all N keys (the unsharded result the
+    USP path must equal), with `rows` sized so the whole run stays within about
+    two minutes."""
     if rank != 0:
         return
-    heads = sample_heads(w)
+    import numpy as np
+    import oracle
+    sub = wl.custom(w.name, w.dtype, w.B, w.ulysses, w.N, w.D, w.ulysses, w.ring, seed=w.seed)
+    inp = wl.make_inputs(sub, with_dout=False)
+    q, k, v = (inp[n][0, 0].double().numpy() for n in ("q", "k", "v"))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, np.arange(256), w.scale)
+    rate = 256 / (time.perf_counter() - t0)               # rows per second
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(16, min(w.N, rate * budget)))
+    g = torch.Generator().manual_seed(w.row_seed)
     times = []
     for i in range(args.warmup + args.steps):
-        dt = run_oracle_sample(w, heads)
+        sel = torch.randint(0, w.N, (rows,), generator=g).numpy()
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, sel, w.scale)
+        dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
-    flop = oracle_sample_flop(w, heads)
+    flop = 4.0 * rows * w.N * w.D
     tflops = flop / statistics.mean(times) / 1e12
-    sample = f"oracle USP forward (numpy fp64) on {heads} of {w.H} heads of {w.name}, full N"
+    sample = (f"oracle attention (numpy fp64) of {rows} seeded query rows of one head against all N={w.N} keys "
+              f"of {w.name}, per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
@@ -204,16 +235,18 @@ class Step:
     def flush(self):
         self.flush_buf.fill_(1)
 
-    def run(self, ev=None):
+    def run(self, ev=None, only=None):
         usp, w = self.usp, self.w
         if ev:
             ev[0].record()
-        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
-                          mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
+        if only in (None, "materialised"):
+            usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                              mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
         if ev:
             ev[1].record()
-        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
-                          mode="fused", out=self.out_f, lse=self.lse_f)
+        if only in (None, "fused"):
+            usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                              mode="fused", out=self.out_f, lse=self.lse_f)
         if ev:
             ev[2].record()
 
@@ -282,21 +315,22 @@ def our_arm(args, w, ws, rank, local):
     usp.lib()
     peaks = load_peaks()
     step = Step(w, backward=False)
-    for _ in range(args.warmup):
-        step.flush()
-        step.run()
-    torch.cuda.synchronize()
-    if usp.device_status() != 0:
-        raise RuntimeError("device error status during warm-up")
-
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    barrier(ws)
-    torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        for _ in range(args.warmup):
+            step.flush()
+            step.run(only=args.only)
+        torch.cuda.synchronize()
+        if usp.device_status() != 0:
+            raise RuntimeError("device error status during warm-up")
+        barrier(ws)
+        torch.cuda.synchronize()
+        clocks.mark("start")
         for i in range(args.steps):
             step.flush()
-            step.run(evs[i])
+            step.run(evs[i], only=args.only)
         torch.cuda.synchronize()
+        clocks.mark("end")
     barrier(ws)
     if usp.device_status() != 0:
         raise RuntimeError("device error status during the timed steps")
@@ -308,7 +342,7 @@ def our_arm(args, w, ws, rank, local):
 
     # end to end through the public call with host buffers
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.only is None:
         for _ in range(2):
             step.run_e2e()
         torch.cuda.synchronize()
@@ -324,7 +358,7 @@ def our_arm(args, w, ws, rank, local):
         e2e = {"value": ws * step.flop() / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
 
-    rows = time_rows(w) if rank == 0 else {}
+    rows = time_rows(w) if (rank == 0 and not args.no_rows) else {}
     if rank != 0:
         return
     fused_s = statistics.mean(fus)
@@ -369,12 +403,15 @@ def our_arm(args, w, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
     ap.add_argument("--workload", default="qwen1024", choices=wl.ORDER)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row GB/s timings")
+    ap.add_argument("--only", choices=["materialised", "fused"], default=None,
+                    help="run one of the two forward calls per step (profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     w = wl.WORKLOADS[args.workload]
