@@ -43,6 +43,8 @@ SIGNATURES = {
                                  _vp, _sz, _vp]),
     "usp_attention_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int,
                                  _f32, _int, _vp, _sz, _vp]),
+    "usp_attention_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _fp, _i64, _i64, _i64, _i64, _int, _int, _f32, _int,
+                                         _vp]),
     "usp_device_status": (_int, [_vp]),
     "usp_status_string": (ctypes.c_char_p, [_int]),
     "usp_last_cuda_error": (_int, []),

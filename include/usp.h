@@ -156,6 +156,26 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
                       int64_t D, int ulysses, int ring, float scale, usp_dtype dtype, void* workspace,
                       size_t workspace_bytes, usp_stream_t stream);
 
+/* The materialised forward (same arguments, layouts, result and errors as
+ * usp_attention_fwd with mode USP_MATERIALISED) for callers that cannot
+ * allocate device memory: code running under a framework whose caching
+ * allocator owns the card, where an extra cudaMalloc can fail or break the
+ * memory budget, and latency-critical callers that must not call
+ * cudaMalloc/cudaFree (which may synchronise the device) on their request
+ * path.  The pages have no counterpart to this call; it exists for such hosts.
+ * Its scratch is one 64 MiB array compiled into the library (every device that
+ * loads libusp holds it until exit).  Problems whose workspace
+ * (usp_attention_workspace_bytes) exceeds 64 MiB return USP_ERR_WORKSPACE.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the array and it keeps the last call's
+ * contents (nothing here needs it zeroed); calls that overlap on the GPU --
+ * other streams or host threads -- race on it and must be serialised by the
+ * caller.  Allocates nothing. */
+int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B,
+                              int64_t H, int64_t N, int64_t D, int ulysses, int ring, float scale,
+                              usp_dtype dtype, usp_stream_t stream);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns USP_OK, USP_ERR_TIMEOUT if a bounded device wait expired
  * since the last call, or USP_ERR_CUDA. */
