@@ -40,6 +40,12 @@ constexpr int TILE_BYTES = BM * HD * 2;   // one 128 x 128 bf16 tile
 constexpr int HALF_BYTES = TILE_BYTES / 2;  // 64-column half (128-byte rows, 128B swizzle)
 constexpr int NUM_THREADS = 384;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+#ifndef USP_REGS_CTRL
+#define USP_REGS_CTRL 56
+#endif
+constexpr int REGS_CTRL = USP_REGS_CTRL;
+constexpr int REGS_SOFTMAX = (NUM_THREADS * 168 - 128 * REGS_CTRL) / 256 / 8 * 8;
+static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= NUM_THREADS * 168, "register split exceeds the launch");
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + 2 * TILE_BYTES;
@@ -187,7 +193,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Guard& G = p.guard;
-
+  // Register split: the producer/MMA warpgroup hands registers to the two
+  // softmax warpgroups (128*REGS_CTRL + 256*REGS_SOFTMAX = 384*168, the
+  // allocation the CTA was launched with).
+  // Each role's code sits inside the branch that set its register budget, so
+  // the compiler allocates every region against the right limit.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REGS_CTRL) : "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -227,24 +239,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tO[2] = {tmem + 256, tmem + 384};
       const uint32_t sQ[2] = {sbase + OFF_Q, sbase + OFF_Q + TILE_BYTES};
       bool ok = ptx::mbar_wait(bar(B_QFULL), 0, G, abort_flag, kDevTimeoutMma);
+      // Descriptors are built once; per-MMA start addresses are added to the
+      // low (address >> 4) field, which cannot carry out of its 14 bits since
+      // shared memory ends below 256 KB.
+      const uint64_t dV0 = ptx::smem_desc_sw128(sbase + OFF_V, HALF_BYTES, 1024);
+      const uint64_t dK0 = ptx::smem_desc_sw128(sbase + OFF_K, 16, 1024);
+      const uint64_t dQ0 = ptx::smem_desc_sw128(sQ[0], 16, 1024);
       auto issue_pv = [&](int i, int jv) {
-        const uint32_t sv = sbase + OFF_V + (jv % KV_STAGES) * TILE_BYTES;
+        const uint64_t dv = ptx::launder(dV0 + (uint64_t)(((jv % KV_STAGES) * TILE_BYTES) >> 4));
+        const uint32_t ts = ptx::launder(tS[i]);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           // B = V tile viewed as [K = keys][N = D]: N-contiguous 128-byte rows,
           // 8-row groups 1024 B apart (SBO), the two 64-column halves 16 KB apart (LBO).
-          const uint64_t bdesc = ptx::smem_desc_sw128(sv + kk * 16 * 128, HALF_BYTES, 1024);
-          ptx::mma_ts(tO[i], tS[i] + kk * 8, bdesc, IDESC_PV, (jv > 0 || kk > 0) ? 1u : 0u);
+          ptx::mma_ts(tO[i], ts + kk * 8, dv + (uint64_t)((kk * 16 * 128) >> 4), IDESC_PV,
+                      (jv > 0 || kk > 0) ? 1u : 0u);
         }
       };
       auto issue_s = [&](int i, int jk) {
-        const uint32_t sk = sbase + OFF_K + (jk % KV_STAGES) * TILE_BYTES;
+        const uint64_t dk = ptx::launder(dK0 + (uint64_t)(((jk % KV_STAGES) * TILE_BYTES) >> 4));
+        const uint64_t dq = ptx::launder(dQ0 + (uint64_t)((i * TILE_BYTES) >> 4));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint32_t off = (kk / 4) * HALF_BYTES + (kk % 4) * 32;
-          const uint64_t adesc = ptx::smem_desc_sw128(sQ[i] + off, 16, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(sk + off, 16, 1024);
-          ptx::mma_ss(tS[i], adesc, bdesc, IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)((((kk / 4) * HALF_BYTES) + (kk % 4) * 32) >> 4);
+          ptx::mma_ss(tS[i], dq + off, dk + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
       for (int j = 0; ok && j < p.kv_tiles; ++j) {
@@ -285,7 +303,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mma_commit(bar(B_MMADONE));
       ptx::mbar_drain(bar(B_MMADONE), 0, 200000000ull);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REGS_SOFTMAX) : "memory");
     // ------------------------------------------------------------ softmax
     const int wg = (warp - 4) / 4;     // query tile owned by this warpgroup
     const int quarter = warp % 4;      // TMEM lanes [32*quarter, 32*quarter + 32)
@@ -304,12 +324,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                                   kDevTimeoutSoftmax));
       if (!ok) break;
       ptx::tc_fence_after();
-      uint32_t sr[128];
-      ptx::tmem_ld32(tS + 0, sr);
-      ptx::tmem_ld32(tS + 32, sr + 32);
-      ptx::tmem_ld32(tS + 64, sr + 64);
-      ptx::tmem_ld32(tS + 96, sr + 96);
-      ptx::tmem_wait_ld();
+      uint32_t sr[BN];
+      ptx::tmem_ld4x32(tS, sr);
       float* s = reinterpret_cast<float*>(sr);
       const int valid = tile_ref(p, j, false).valid;
       if (valid < BN) {
@@ -317,10 +333,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= valid) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      // row maximum as a tree (depth 7 instead of a 128-long chain)
+      float mx[16];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_tile = mx * sl2;
+      for (int c = 0; c < 16; ++c)
+        mx[c] = fmaxf(fmaxf(fmaxf(s[c], s[c + 16]), fmaxf(s[c + 32], s[c + 48])),
+                      fmaxf(fmaxf(s[c + 64], s[c + 80]), fmaxf(s[c + 96], s[c + 112])));
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+      const float m_tile = mx[0] * sl2;
       const bool need = m_tile > m + RESCALE_THRESHOLD;
       const float m_new = need ? m_tile : m;
       if (j > 0 && __any_sync(0xffffffffu, need)) {
@@ -329,7 +352,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
           ptx::tmem_ld32(tO + cc * 32, o);
-          ptx::tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
           ptx::tmem_st32(tO + cc * 32, o);
@@ -340,20 +362,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         l *= ptx::ex2(m - m_new);
         m = m_new;
       }
-      float rs = 0.f;
+      // P = exp2(S*scale*log2e - m), packed to bf16 pairs 32 columns at a time
+      float ps[8];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+      for (int c = 0; c < 8; ++c) ps[c] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ptx::ex2(fmaf(s[half * 64 + 2 * c], sl2, -m));
-          const float p1 = ptx::ex2(fmaf(s[half * 64 + 2 * c + 1], sl2, -m));
-          rs += p0 + p1;
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          const float p0 = ptx::ex2(fmaf(s[q4 * 32 + 2 * c], sl2, -m));
+          const float p1 = ptx::ex2(fmaf(s[q4 * 32 + 2 * c + 1], sl2, -m));
+          ps[c & 7] += p0 + p1;
           pk[c] = pack_bf16(p0, p1);
         }
-        ptx::tmem_st32(tS + half * 32, pk);
+        ptx::tmem_st16(tS + q4 * 16, pk);
       }
-      l += rs;
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(B_PFULL + wg));
