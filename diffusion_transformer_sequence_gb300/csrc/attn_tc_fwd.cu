@@ -333,16 +333,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= valid) s[c] = -INFINITY;
       }
-      // row maximum as a tree (depth 7 instead of a 128-long chain)
-      float mx[16];
+      // row maximum: a tree of 3-input max (64 instructions, depth 5)
+      float mx[43];
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        mx[c] = fmaxf(fmaxf(fmaxf(s[c], s[c + 16]), fmaxf(s[c + 32], s[c + 48])),
-                      fmaxf(fmaxf(s[c + 64], s[c + 80]), fmaxf(s[c + 96], s[c + 112])));
-#pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
-#pragma unroll
-        for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+      for (int c = 0; c < 42; ++c) mx[c] = ptx::max3(s[3 * c], s[3 * c + 1], s[3 * c + 2]);
+      mx[42] = fmaxf(s[126], s[127]);
+      mx[0] = ptx::MaxTree<43>::run(mx);
       const float m_tile = mx[0] * sl2;
       const bool need = m_tile > m + RESCALE_THRESHOLD;
       const float m_new = need ? m_tile : m;
@@ -362,23 +358,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         l *= ptx::ex2(m - m_new);
         m = m_new;
       }
-      // P = exp2(S*scale*log2e - m), packed to bf16 pairs 32 columns at a time
-      float ps[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) ps[c] = 0.f;
+      // P = exp2(S*scale*log2e - m): the affine step on packed fp32 pairs, the
+      // exponential on the MUFU, bf16 packing, 32 columns per TMEM store.
+      const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2);
+      const uint64_t negm2 = ptx::f2_pack(-m, -m);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
-          const float p0 = ptx::ex2(fmaf(s[q4 * 32 + 2 * c], sl2, -m));
-          const float p1 = ptx::ex2(fmaf(s[q4 * 32 + 2 * c + 1], sl2, -m));
-          ps[c & 7] += p0 + p1;
-          pk[c] = pack_bf16(p0, p1);
+          const int col = q4 * 32 + 2 * c;
+          float x0, x1;
+          ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(s[col], s[col + 1]), sl2x2, negm2), x0, x1);
+          const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+          acc[c & 3] = ptx::f2_add(acc[c & 3], ptx::f2_pack(p0, p1));
+          pk[c] = ptx::bf16x2(p0, p1);
         }
         ptx::tmem_st16(tS + q4 * 16, pk);
       }
-      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      {
+        float a0, a1;
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_add(acc[0], acc[1]), ptx::f2_add(acc[2], acc[3])), a0, a1);
+        l += a0 + a1;
+      }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(B_PFULL + wg));

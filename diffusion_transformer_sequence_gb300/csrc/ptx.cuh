@@ -243,6 +243,63 @@ __device__ __forceinline__ uint32_t launder(uint32_t x) {
   return y;
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Packed pairs of fp32 (one 64-bit register pair, low word = first element).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Round two fp32 to bf16 (nearest even) and pack: `lo` in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Maximum of N floats as a tree of 3-input max instructions (depth log3 N).
+template <int N>
+struct MaxTree {
+  static __device__ __forceinline__ float run(float* v) {
+    constexpr int M = N / 3, R = N % 3;
+#pragma unroll
+    for (int i = 0; i < M; ++i) v[i] = max3(v[3 * i], v[3 * i + 1], v[3 * i + 2]);
+#pragma unroll
+    for (int i = 0; i < R; ++i) v[M + i] = v[3 * M + i];
+    return MaxTree<M + R>::run(v);
+  }
+};
+template <>
+struct MaxTree<1> {
+  static __device__ __forceinline__ float run(float* v) { return v[0]; }
+};
+template <>
+struct MaxTree<2> {
+  static __device__ __forceinline__ float run(float* v) { return fmaxf(v[0], v[1]); }
+};
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
