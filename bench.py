@@ -120,7 +120,8 @@ def dist_env():
 def max_over_ranks(x: float, ws: int) -> float:
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 
@@ -175,9 +176,10 @@ def reference_arm(args, w, ws, rank):
     sub = wl.custom(w.name, w.dtype, w.B, w.ulysses, w.N, w.D, w.ulysses, w.ring, seed=w.seed)
     inp = wl.make_inputs(sub, with_dout=False)
     q, k, v = (inp[n][0, 0].double().numpy() for n in ("q", "k", "v"))
+    ncal = min(256, w.N)
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, np.arange(256), w.scale)
-    rate = 256 / (time.perf_counter() - t0)               # rows per second
+    oracle.attention_rows(q, k, v, np.arange(ncal), w.scale)
+    rate = ncal / (time.perf_counter() - t0)              # rows per second
     budget = 120.0 / max(1, args.steps + args.warmup)
     rows = int(max(16, min(w.N, rate * budget)))
     g = torch.Generator().manual_seed(w.row_seed)
