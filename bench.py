@@ -225,8 +225,15 @@ class Step:
         nws = usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, "materialised")
         self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
         self.backward = backward
+        if backward:
+            nb = usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, backward=True)
+            self.ws_b = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            self.grads = [torch.empty_like(self.dev["q"]) for _ in range(3)]
+            # the backward consumes the fused forward's out / lse: make them valid once up front
+            usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
+                              mode="fused", out=self.out_f, lse=self.lse_f)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-        self.launches_per_step = (7 if w.ring > 1 else 6) + 1
+        self.launches_per_step = (7 if w.ring > 1 else 6) + 1 + (3 if backward else 0)
 
     def flop(self):
         f = 2 * self.w.fwd_flop
@@ -251,6 +258,22 @@ class Step:
                               mode="fused", out=self.out_f, lse=self.lse_f)
         if ev:
             ev[2].record()
+        if self.backward and only in (None, "backward"):
+            self.bwd()
+        if ev:
+            ev[3].record()
+
+    def bwd(self):
+        usp, w = self.usp, self.w
+        L = usp.lib()
+        from diffusion_transformer_sequence_gb300 import _lib
+        d = self.dev
+        rc = L.usp_attention_bwd(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(), self.out_f.data_ptr(),
+                                 self.lse_f.data_ptr(), d["dout"].data_ptr(), self.grads[0].data_ptr(),
+                                 self.grads[1].data_ptr(), self.grads[2].data_ptr(), w.B, w.H, w.N, w.D, w.ulysses,
+                                 w.ring, w.scale, _lib.USP_BF16 if w.dtype == "bf16" else _lib.USP_F32,
+                                 self.ws_b.data_ptr(), self.ws_b.numel(), torch.cuda.current_stream().cuda_stream)
+        _lib.check("usp_attention_bwd", rc)
 
     def run_e2e(self):
         """Host buffers in and out: H2D of q, k, v, the step, D2H of the outputs."""
@@ -261,7 +284,12 @@ class Step:
                           mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
         usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
                           mode="fused", out=self.out_f, lse=self.lse_f)
-        for name, t in (("out_m", self.out_m), ("lse_m", self.lse_m), ("out_f", self.out_f), ("lse_f", self.lse_f)):
+        outs = [("out_m", self.out_m), ("lse_m", self.lse_m), ("out_f", self.out_f), ("lse_f", self.lse_f)]
+        if self.backward:
+            self.dev["dout"].copy_(self.host["dout"], non_blocking=True)
+            self.bwd()
+            outs += [("dq", self.grads[0]), ("dk", self.grads[1]), ("dv", self.grads[2])]
+        for name, t in outs:
             dst = getattr(self, "h_" + name, None)
             if dst is None:
                 dst = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
@@ -269,8 +297,11 @@ class Step:
             dst.copy_(t, non_blocking=True)
 
     def io_bytes(self):
-        h2d = sum(self.host[n].numel() * self.host[n].element_size() for n in ("q", "k", "v"))
+        names = ("q", "k", "v", "dout") if self.backward else ("q", "k", "v")
+        h2d = sum(self.host[n].numel() * self.host[n].element_size() for n in names)
         d2h = 2 * (self.out_m.numel() * self.out_m.element_size() + self.lse_m.numel() * 4)
+        if self.backward:
+            d2h += sum(g.numel() * g.element_size() for g in self.grads)
         return h2d, d2h
 
 
@@ -316,8 +347,8 @@ def our_arm(args, w, ws, rank, local):
     import diffusion_transformer_sequence_gb300 as usp
     usp.lib()
     peaks = load_peaks()
-    step = Step(w, backward=False)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    step = Step(w, backward=not args.no_backward)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
         for _ in range(args.warmup):
             step.flush()
@@ -338,7 +369,8 @@ def our_arm(args, w, ws, rank, local):
         raise RuntimeError("device error status during the timed steps")
     mat = [e[0].elapsed_time(e[1]) * 1e-3 for e in evs]
     fus = [e[1].elapsed_time(e[2]) * 1e-3 for e in evs]
-    step_s = sum(m + f for m, f in zip(mat, fus)) / args.steps
+    bwd = [e[2].elapsed_time(e[3]) * 1e-3 for e in evs]
+    step_s = sum(e[0].elapsed_time(e[3]) * 1e-3 for e in evs) / args.steps
     step_s = max_over_ranks(step_s, ws)
     value = ws * step.flop() / step_s / 1e12
 
@@ -386,10 +418,13 @@ def our_arm(args, w, ws, rank, local):
         "config": {"workload": w.name, "desc": w.description, "global_batch": w.B * ws, "seq_len": w.N,
                    "heads": w.H, "head_dim": w.D, "ulysses": w.ulysses, "ring": w.ring,
                    "parallelism": f"{ws} independent replicas; u x r virtual ranks per device",
-                   "step": "usp_attention_fwd materialised + usp_attention_fwd fused",
+                   "step": "usp_attention_fwd materialised + usp_attention_fwd fused"
+                           + (" + usp_attention_bwd" if step.backward else ""),
                    "l2": "flushed (256 MB write) before every timed step, outside the events"},
         "rows": {"materialised_fwd_ms": mat_s * 1e3, "fused_fwd_ms": fused_s * 1e3,
                  "materialised_fwd_tflops": w.fwd_flop / mat_s / 1e12, "fused_fwd_tflops": fused_tflops,
+                 **({"bwd_ms": statistics.mean(bwd) * 1e3,
+                     "bwd_tflops": w.bwd_flop / statistics.mean(bwd) / 1e12} if step.backward else {}),
                  **{k + "_GBps": v["GB/s"] for k, v in rows.items()},
                  **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items()}},
         "roofline": roofline,
@@ -412,7 +447,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row GB/s timings")
-    ap.add_argument("--only", choices=["materialised", "fused"], default=None,
+    ap.add_argument("--no-backward", action="store_true", help="leave usp_attention_bwd out of the step")
+    ap.add_argument("--only", choices=["materialised", "fused", "backward"], default=None,
                     help="run one of the two forward calls per step (profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_env()

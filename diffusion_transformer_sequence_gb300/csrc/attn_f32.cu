@@ -140,7 +140,140 @@ cudaError_t dispatch(const float* q, const float* k, const float* v, float* out,
   return launch_dmax<128>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
 }
 
+// ---------------------------------------------------------------- backward
+// Delta_i = sum_d dO_id O_id, one warp per row, shuffle reduction.
+__global__ void __launch_bounds__(256) f32_bwd_delta_kernel(const float* __restrict__ out,
+                                                            const float* __restrict__ dout, float* __restrict__ delta,
+                                                            int64_t rows, int D) {
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (row >= rows) return;
+  float acc = 0.f;
+  for (int d = lane; d < D; d += 32) acc = fmaf(out[row * D + d], dout[row * D + d], acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) delta[row] = acc;
+}
+
+// One warp per "own" row (a query row for dQ, a key row for dK/dV); the other
+// side streams through shared memory 32 rows at a time, lane l taking row l.
+//   dQ_i  = scale sum_j P_ij (dP_ij - Delta_i) k_j
+//   dV_j  = sum_i P_ij dO_i,   dK_j = scale sum_i P_ij (dP_ij - Delta_i) q_i
+// with P_ij = exp(scale q_i.k_j - lse_i), dP_ij = dO_i . v_j.
+template <int kDmax, bool kDQ>
+__global__ void __launch_bounds__(kWarps * 32) f32_bwd_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const float* __restrict__ lse, const float* __restrict__ delta, const float* __restrict__ dout,
+    float* __restrict__ g0, float* __restrict__ g1, int64_t N, int D, float scale, F32Addr addr) {
+  __shared__ float A[kTileK][kDmax + 1];  // streamed: k (dQ) or q (dK/dV)
+  __shared__ float Bs[kTileK][kDmax + 1]; // streamed: v (dQ) or dO (dK/dV)
+  __shared__ float Ls[kTileK], Ds[kTileK];
+  __shared__ float Own0[kWarps][kDmax], Own1[kWarps][kDmax];
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t head = blockIdx.y;
+  const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
+  const bool active = row < N;
+  float own_l = 0.f, own_d = 0.f;
+  if (active) {
+    const int64_t off = addr.row_off(head, row, N, D);
+    for (int d = lane; d < D; d += 32) {
+      Own0[warp][d] = kDQ ? q[off + d] : k[off + d];
+      Own1[warp][d] = kDQ ? dout[off + d] : v[off + d];
+    }
+    if (kDQ) {
+      own_l = lse[addr.lse_off(head, row, N)];
+      own_d = delta[addr.lse_off(head, row, N)];
+    }
+  }
+  float acc0[kDmax / 32], acc1[kDmax / 32];
+#pragma unroll
+  for (int i = 0; i < kDmax / 32; ++i) acc0[i] = acc1[i] = 0.f;
+  for (int64_t j0 = 0; j0 < N; j0 += kTileK) {
+    __syncthreads();
+    const int nt = (int)((N - j0) < kTileK ? (N - j0) : kTileK);
+    for (int e = threadIdx.x; e < kTileK * D; e += blockDim.x) {
+      const int jj = e / D, d = e - jj * D;
+      float a = 0.f, b = 0.f;
+      if (jj < nt) {
+        const int64_t off = addr.row_off(head, j0 + jj, N, D) + d;
+        a = kDQ ? k[off] : q[off];
+        b = kDQ ? v[off] : dout[off];
+      }
+      A[jj][d] = a;
+      Bs[jj][d] = b;
+    }
+    if (!kDQ && threadIdx.x < kTileK) {
+      const int jj = threadIdx.x;
+      Ls[jj] = jj < nt ? lse[addr.lse_off(head, j0 + jj, N)] : 0.f;
+      Ds[jj] = jj < nt ? delta[addr.lse_off(head, j0 + jj, N)] : 0.f;
+    }
+    __syncthreads();
+    if (!active) continue;
+    float p = 0.f, ds = 0.f;
+    if (lane < nt) {
+      float s = 0.f, dp = 0.f;
+      for (int d = 0; d < D; ++d) {
+        s = fmaf(Own0[warp][d], A[lane][d], s);
+        dp = fmaf(kDQ ? Own1[warp][d] : Bs[lane][d], kDQ ? Bs[lane][d] : Own1[warp][d], dp);
+      }
+      const float l = kDQ ? own_l : Ls[lane];
+      const float dl = kDQ ? own_d : Ds[lane];
+      p = expf(s * scale - l);
+      ds = p * (dp - dl);
+    }
+    for (int jj = 0; jj < nt; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+      const float dsj = __shfl_sync(0xffffffffu, ds, jj);
+#pragma unroll
+      for (int i = 0; i < kDmax / 32; ++i) {
+        const int d = lane + 32 * i;
+        if (d < D) {
+          if (kDQ) {
+            acc0[i] = fmaf(dsj, A[jj][d], acc0[i]);             // dQ += dS k
+          } else {
+            acc0[i] = fmaf(dsj, A[jj][d], acc0[i]);             // dK += dS q
+            acc1[i] = fmaf(pj, Bs[jj][d], acc1[i]);             // dV += P dO
+          }
+        }
+      }
+    }
+  }
+  if (!active) return;
+  const int64_t off = addr.row_off(head, row, N, D);
+#pragma unroll
+  for (int i = 0; i < kDmax / 32; ++i) {
+    const int d = lane + 32 * i;
+    if (d < D) {
+      g0[off + d] = acc0[i] * scale;
+      if (!kDQ) g1[off + d] = acc1[i];
+    }
+  }
+}
+
+template <int kDmax>
+cudaError_t launch_bwd_dmax(const float* q, const float* k, const float* v, const float* out, const float* lse,
+                            const float* dout, float* dq, float* dk, float* dv, float* delta, int64_t BH, int64_t N,
+                            int D, float scale, F32Addr addr, cudaStream_t stream) {
+  const int64_t rows = BH * N;
+  f32_bwd_delta_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, stream>>>(out, dout, delta, rows, D);
+  dim3 grid((unsigned)((N + kWarps - 1) / kWarps), (unsigned)BH, 1);
+  f32_bwd_kernel<kDmax, true><<<grid, kWarps * 32, 0, stream>>>(q, k, v, lse, delta, dout, dq, nullptr, N, D, scale, addr);
+  f32_bwd_kernel<kDmax, false><<<grid, kWarps * 32, 0, stream>>>(q, k, v, lse, delta, dout, dk, dv, N, D, scale, addr);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, const float* out,
+                                const float* lse, const float* dout, float* dq, float* dk, float* dv,
+                                float* delta, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
+                                cudaStream_t stream) {
+  F32Addr addr{true, BH, Ns};
+  const int64_t N = sp * Ns;
+  if (D <= 32) return launch_bwd_dmax<32>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
+  if (D <= 64) return launch_bwd_dmax<64>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
+  return launch_bwd_dmax<128>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
+}
 
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* out, float* lse,
                             int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,

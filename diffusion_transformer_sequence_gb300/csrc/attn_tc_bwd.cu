@@ -1,0 +1,560 @@
+// bf16 USP attention backward on the tcgen05 tensor cores (D = 128).
+//
+// What it computes ("Feat: USP sequence parallelism (Ulysses x Ring) via
+// SequenceParallelPlan; Wan enabled", Numerics and "Ring kernel selection":
+// the forward returns the LSE and pairs with a real backward; every ring step
+// uses its own KV chunk and the MERGED LSE).  With P = exp(scale q k^T - lse):
+//   Delta_i = sum_d dO_id O_id,  dP = dO V^T,  dS = P * (dP - Delta),
+//   dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
+// The kernels read the token-sharded stacks [sp][B*H][Ns][D] in place through
+// 4-D tensor maps (the same addressing as the fused forward), so the Ulysses
+// re-layout and the ring rotation are addressing, and each KV chunk's dK/dV
+// accumulates over every query shard -- every (rank, ring step) pair -- inside
+// one CTA, in a fixed order.  No atomics: the gradients are bitwise
+// reproducible run to run.
+//
+//   usp_bwd_prep_kernel   Delta = rowsum(dO * O) and L2 = lse * log2(e), fp32
+//   usp_bwd_dkdv_kernel   one CTA per (head, 128-key tile); loops over every
+//                         128-query tile: S^T = K Q^T, dP^T = V dO^T (TMEM),
+//                         P^T, dS^T in registers -> bf16 back into TMEM,
+//                         dV += P^T dO, dK += dS^T Q (TMEM accumulators)
+//   usp_bwd_dq_kernel     one CTA per (head, 128-query tile); loops over every
+//                         key tile: S = Q K^T, dP = dO V^T, dS -> TMEM,
+//                         dQ += dS K
+// Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
+// warps 4..11 two elementwise warpgroups; warpgroup w owns columns
+// [64w, 64w + 64) of every S / dP row (a thread owns one TMEM lane = one row).
+// Each warpgroup writes its packed bf16 results back inside its own column
+// range, so no thread overwrites TMEM another thread still has to read.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "ptx.cuh"
+#include "usp_internal.cuh"
+
+namespace usp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int HD = 128;
+constexpr int TILE_BYTES = BM * HD * 2;
+constexpr int HALF_BYTES = TILE_BYTES / 2;
+constexpr int VEC_BYTES = BM * 4;  // 128 fp32 (L2 or Delta of one tile)
+constexpr int NUM_THREADS = 384;
+constexpr int STAGES = 2;
+constexpr int REGS_CTRL = 56;
+constexpr int REGS_ELEM = (NUM_THREADS * 168 - 128 * REGS_CTRL) / 256 / 8 * 8;
+constexpr float LOG2E = 1.4426950408889634f;
+
+struct BwdParams {
+  void* dst0;          // dkdv: dK   | dq: dQ
+  void* dst1;          // dkdv: dV   | dq: unused
+  const float* l2;     // lse * log2(e), [sp][BH][Ns]
+  const float* delta;  // rowsum(dO * O), [sp][BH][Ns]
+  int64_t BH, Ns;
+  int64_t Ns_pad;      // row pitch of l2 / delta (Ns rounded up to 4: 16-byte rows for TMA)
+  int tiles_per_seg;
+  int tiles;           // tiles per head (sp * tiles_per_seg)
+  float scale, scale_log2;
+  Guard guard;
+};
+
+struct TileRef {
+  int row0, seg, valid;
+};
+__device__ __forceinline__ TileRef tile_ref(const BwdParams& p, int tile) {
+  TileRef t;
+  t.seg = tile / p.tiles_per_seg;
+  t.row0 = (tile - t.seg * p.tiles_per_seg) * BM;
+  const int64_t rem = p.Ns - t.row0;
+  t.valid = rem < BM ? (int)rem : BM;
+  return t;
+}
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, uint32_t dst, uint32_t bar, int64_t bh,
+                                          const TileRef& t) {
+  ptx::tma_load_4d(dst, map, bar, 0, t.row0, (int)bh, t.seg);
+  ptx::tma_load_4d(dst + HALF_BYTES, map, bar, 64, t.row0, (int)bh, t.seg);
+}
+__device__ __forceinline__ int64_t row_index(const BwdParams& p, int64_t bh, const TileRef& t, int r) {
+  return ((int64_t)t.seg * p.BH + bh) * p.Ns + t.row0 + r;
+}
+__device__ __forceinline__ int64_t vec_index(const BwdParams& p, int64_t bh, const TileRef& t, int r) {
+  return ((int64_t)t.seg * p.BH + bh) * p.Ns_pad + t.row0 + r;
+}
+
+// Shared-memory layout (both kernels): two resident tiles A0, A1, then
+// STAGES x (two streamed tiles + two fp32 vectors), then barriers.
+constexpr int OFF_A0 = 0;
+constexpr int OFF_A1 = TILE_BYTES;
+constexpr int OFF_STAGE = 2 * TILE_BYTES;
+constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * VEC_BYTES;
+constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
+constexpr int B_RES = 0;                 // resident tiles loaded
+constexpr int B_FULL = 1;                // + stage
+constexpr int B_EMPTY = B_FULL + STAGES;  // + stage
+constexpr int B_SFULL = B_EMPTY + STAGES;
+constexpr int B_PFULL = B_SFULL + 1;
+constexpr int B_ODONE = B_PFULL + 1;
+constexpr int B_MMADONE = B_ODONE + 1;
+constexpr int NUM_BARS = B_MMADONE + 1;
+constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
+constexpr int OFF_ABORT = OFF_SLOT + 8;
+constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;
+
+__device__ __forceinline__ uint32_t stage_addr(uint32_t sbase, int s) { return sbase + OFF_STAGE + s * STAGE_BYTES; }
+
+// 64 columns per lane: two 32-column loads, one wait.
+__device__ __forceinline__ void ld64(uint32_t taddr, uint32_t* r) { ptx::tmem_ld64(taddr, r); }
+
+// Common prologue: barriers, TMEM, register split.  Returns the TMEM base.
+__device__ __forceinline__ uint32_t prologue(uint8_t* smem, uint32_t sbase, int warp, int lane, uint32_t pfull_count) {
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(B_RES), 1);
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(bar(B_FULL + s), 1);
+      ptx::mbar_init(bar(B_EMPTY + s), 1);
+    }
+    ptx::mbar_init(bar(B_SFULL), 1);
+    ptx::mbar_init(bar(B_PFULL), pfull_count);
+    ptx::mbar_init(bar(B_ODONE), 1);
+    ptx::mbar_init(bar(B_MMADONE), 1);
+    *reinterpret_cast<volatile int*>(smem + OFF_ABORT) = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + OFF_SLOT, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  return *reinterpret_cast<uint32_t*>(smem + OFF_SLOT);
+}
+
+__device__ __forceinline__ void teardown(uint32_t tmem, int warp) {
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// Store 64 fp32 columns of one row (times `mul`) as bf16 to global.  Every
+// lane of the warp runs the (warp-collective) TMEM loads; only lanes with
+// `store` set write.
+__device__ __forceinline__ void store_row64(__nv_bfloat16* dst, uint32_t taddr, float mul, bool store) {
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    uint32_t o[32];
+    ptx::tmem_ld32(taddr + cc * 32, o);
+    uint32_t pk[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) pk[c] = ptx::bf16x2(__uint_as_float(o[2 * c]) * mul, __uint_as_float(o[2 * c + 1]) * mul);
+    if (store) {
+      uint4* d = reinterpret_cast<uint4*>(dst + cc * 32);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) d[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+  }
+}
+
+// A operand columns (packed bf16) of k-step kk: warpgroup 0 wrote keys/queries
+// [0,64) at columns [0,32), warpgroup 1 wrote [64,128) at [64,96).
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+
+// =====================================================================
+// dK, dV: one CTA per (head, key tile); resident K (A0), V (A1); streamed
+// Q, dO, L2, Delta per query tile.
+// TMEM: S^T [0,128)  dP^T [128,256)  dV [256,384)  dK [384,512).
+// =====================================================================
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    usp_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                        const __grid_constant__ CUtensorMap tm_l2, const __grid_constant__ CUtensorMap tm_dl,
+                        const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t bh = blockIdx.y;
+  const TileRef kt = tile_ref(p, blockIdx.x);
+  const Guard& G = p.guard;
+  const uint32_t tmem = prologue(smem, sbase, warp, lane, 256);
+  const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REGS_CTRL) : "memory");
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      ptx::mbar_arrive_expect_tx(bar(B_RES), 2 * TILE_BYTES);
+      load_tile(&tm_k, sbase + OFF_A0, bar(B_RES), bh, kt);
+      load_tile(&tm_v, sbase + OFF_A1, bar(B_RES), bh, kt);
+      int issued = 0;
+      for (int i = 0; i < p.tiles; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (uint32_t)((i / STAGES) & 1);
+        if (!ptx::mbar_wait(bar(B_EMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
+        const TileRef qt = tile_ref(p, i);
+        const uint32_t st = stage_addr(sbase, s);
+        ptx::mbar_arrive_expect_tx(bar(B_FULL + s), 2 * TILE_BYTES + 2 * VEC_BYTES);
+        load_tile(&tm_q, st, bar(B_FULL + s), bh, qt);
+        load_tile(&tm_do, st + TILE_BYTES, bar(B_FULL + s), bh, qt);
+        ptx::tma_load_3d(st + 2 * TILE_BYTES, &tm_l2, bar(B_FULL + s), qt.row0, (int)bh, qt.seg);
+        ptx::tma_load_3d(st + 2 * TILE_BYTES + VEC_BYTES, &tm_dl, bar(B_FULL + s), qt.row0, (int)bh, qt.seg);
+        issued = i + 1;
+      }
+      ptx::mbar_drain(bar(B_RES), 0, 200000000ull);
+      for (int i = issued - STAGES; i < issued; ++i)
+        if (i >= 0) ptx::mbar_drain(bar(B_FULL + i % STAGES), (uint32_t)((i / STAGES) & 1), 200000000ull);
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      constexpr uint32_t ID_KMAJ = ptx::idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
+      constexpr uint32_t ID_BMN = ptx::idesc_bf16_f32(BM, HD, 0, 1);   // dV, dK (B = dO / Q, N-major)
+      const uint64_t dK0 = ptx::smem_desc_sw128(sbase + OFF_A0, 16, 1024);
+      const uint64_t dV0 = ptx::smem_desc_sw128(sbase + OFF_A1, 16, 1024);
+      bool ok = ptx::mbar_wait(bar(B_RES), 0, G, abort_flag, kDevTimeoutMma);
+      for (int i = 0; ok && i < p.tiles; ++i) {
+        const int s = i % STAGES;
+        if (!(ok = ptx::mbar_wait(bar(B_FULL + s), (uint32_t)((i / STAGES) & 1), G, abort_flag, kDevTimeoutMma))) break;
+        ptx::tc_fence_after();
+        const uint32_t st = stage_addr(sbase, s);
+        const uint64_t dq = ptx::launder(ptx::smem_desc_sw128(st, 16, 1024));
+        const uint64_t ddo = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, 16, 1024));
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t off = (uint64_t)((((kk / 4) * HALF_BYTES) + (kk % 4) * 32) >> 4);
+          ptx::mma_ss(tSt, dK0 + off, dq + off, ID_KMAJ, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t off = (uint64_t)((((kk / 4) * HALF_BYTES) + (kk % 4) * 32) >> 4);
+          ptx::mma_ss(tdPt, dV0 + off, ddo + off, ID_KMAJ, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(B_SFULL));
+        if (!(ok = ptx::mbar_wait(bar(B_PFULL), (uint32_t)(i & 1), G, abort_flag, kDevTimeoutMma))) break;
+        ptx::tc_fence_after();
+        const uint64_t bdo = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, HALF_BYTES, 1024));
+        const uint64_t bq = ptx::launder(ptx::smem_desc_sw128(st, HALF_BYTES, 1024));
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO (K = queries)
+          ptx::mma_ts(tdV, tSt + packed_col(kk), bdo + (uint64_t)((kk * 2048) >> 4), ID_BMN,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q
+          ptx::mma_ts(tdK, tdPt + packed_col(kk), bq + (uint64_t)((kk * 2048) >> 4), ID_BMN,
+                      (i > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(B_EMPTY + s));
+      }
+      if (ok) ptx::mma_commit(bar(B_ODONE));
+      ptx::mma_commit(bar(B_MMADONE));
+      ptx::mbar_drain(bar(B_MMADONE), 0, 200000000ull);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REGS_ELEM) : "memory");
+    // ------------------------------------------------------------ elementwise
+    const int wg = (warp - 4) / 4;
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;  // key row of this thread
+    const uint32_t lane_bits = (uint32_t)(quarter * 32) << 16;
+    const int c0 = wg * 64;               // query columns of this warpgroup
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < p.tiles; ++i) {
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_SFULL), (uint32_t)(i & 1), G, abort_flag, kDevTimeoutSoftmax));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const uint32_t st = stage_addr(sbase, i % STAGES);
+      const float* l2 = reinterpret_cast<const float*>(smem + (st - sbase) + 2 * TILE_BYTES) + c0;
+      const float* dl = reinterpret_cast<const float*>(smem + (st - sbase) + 2 * TILE_BYTES + VEC_BYTES) + c0;
+      uint32_t sr[64], dr[64];
+      ld64(tSt + lane_bits + c0, sr);
+      ld64(tdPt + lane_bits + c0, dr);
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float x0, x1, y0, y1, d0, d1;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])),
+                                   ptx::f2_pack(sl2, sl2), ptx::f2_pack(-l2[2 * c], -l2[2 * c + 1])),
+                       x0, x1);
+        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])),
+                                   ptx::f2_pack(-dl[2 * c], -dl[2 * c + 1])),
+                       y0, y1);
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), ptx::f2_pack(y0, y1)), d0, d1);
+        pk[c] = ptx::bf16x2(p0, p1);
+        dk[c] = ptx::bf16x2(d0, d1);
+      }
+      ptx::tmem_st32(tSt + lane_bits + c0, pk);
+      ptx::tmem_st32(tdPt + lane_bits + c0, dk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(B_PFULL));
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
+    if (ok) {
+      ptx::tc_fence_after();
+      const bool store = row < kt.valid;
+      const int64_t r = row_index(p, bh, kt, store ? row : 0);
+      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst1) + r * HD + c0, tdV + lane_bits + c0, 1.f, store);
+      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst0) + r * HD + c0, tdK + lane_bits + c0, p.scale, store);
+    }
+  }
+  teardown(tmem, warp);
+}
+
+// =====================================================================
+// dQ: one CTA per (head, query tile); resident Q (A0), dO (A1); streamed
+// K, V per key tile.  TMEM: S [0,128)  dP [128,256)  dQ [256,384).
+// =====================================================================
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    usp_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                      const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = ptx::smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int64_t bh = blockIdx.y;
+  const TileRef qt = tile_ref(p, blockIdx.x);
+  const Guard& G = p.guard;
+  const uint32_t tmem = prologue(smem, sbase, warp, lane, 256);
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REGS_CTRL) : "memory");
+    if (warp == 0 && lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar(B_RES), 2 * TILE_BYTES);
+      load_tile(&tm_q, sbase + OFF_A0, bar(B_RES), bh, qt);
+      load_tile(&tm_do, sbase + OFF_A1, bar(B_RES), bh, qt);
+      int issued = 0;
+      for (int j = 0; j < p.tiles; ++j) {
+        const int s = j % STAGES;
+        const uint32_t ph = (uint32_t)((j / STAGES) & 1);
+        if (!ptx::mbar_wait(bar(B_EMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
+        const TileRef kt = tile_ref(p, j);
+        const uint32_t st = stage_addr(sbase, s);
+        ptx::mbar_arrive_expect_tx(bar(B_FULL + s), 2 * TILE_BYTES);
+        load_tile(&tm_k, st, bar(B_FULL + s), bh, kt);
+        load_tile(&tm_v, st + TILE_BYTES, bar(B_FULL + s), bh, kt);
+        issued = j + 1;
+      }
+      ptx::mbar_drain(bar(B_RES), 0, 200000000ull);
+      for (int j = issued - STAGES; j < issued; ++j)
+        if (j >= 0) ptx::mbar_drain(bar(B_FULL + j % STAGES), (uint32_t)((j / STAGES) & 1), 200000000ull);
+    } else if (warp == 1 && lane == 0) {
+      constexpr uint32_t ID_KMAJ = ptx::idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
+      constexpr uint32_t ID_BMN = ptx::idesc_bf16_f32(BM, HD, 0, 1);   // dQ (B = K, N-major)
+      const uint64_t dQ0 = ptx::smem_desc_sw128(sbase + OFF_A0, 16, 1024);
+      const uint64_t dO0 = ptx::smem_desc_sw128(sbase + OFF_A1, 16, 1024);
+      bool ok = ptx::mbar_wait(bar(B_RES), 0, G, abort_flag, kDevTimeoutMma);
+      for (int j = 0; ok && j < p.tiles; ++j) {
+        const int s = j % STAGES;
+        if (!(ok = ptx::mbar_wait(bar(B_FULL + s), (uint32_t)((j / STAGES) & 1), G, abort_flag, kDevTimeoutMma))) break;
+        ptx::tc_fence_after();
+        const uint32_t st = stage_addr(sbase, s);
+        const uint64_t dk = ptx::launder(ptx::smem_desc_sw128(st, 16, 1024));
+        const uint64_t dv = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, 16, 1024));
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t off = (uint64_t)((((kk / 4) * HALF_BYTES) + (kk % 4) * 32) >> 4);
+          ptx::mma_ss(tS, dQ0 + off, dk + off, ID_KMAJ, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t off = (uint64_t)((((kk / 4) * HALF_BYTES) + (kk % 4) * 32) >> 4);
+          ptx::mma_ss(tdP, dO0 + off, dv + off, ID_KMAJ, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar(B_SFULL));
+        if (!(ok = ptx::mbar_wait(bar(B_PFULL), (uint32_t)(j & 1), G, abort_flag, kDevTimeoutMma))) break;
+        ptx::tc_fence_after();
+        const uint64_t bk = ptx::launder(ptx::smem_desc_sw128(st, HALF_BYTES, 1024));
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dQ += dS K (K = keys)
+          ptx::mma_ts(tdQ, tS + packed_col(kk), bk + (uint64_t)((kk * 2048) >> 4), ID_BMN,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(B_EMPTY + s));
+      }
+      if (ok) ptx::mma_commit(bar(B_ODONE));
+      ptx::mma_commit(bar(B_MMADONE));
+      ptx::mbar_drain(bar(B_MMADONE), 0, 200000000ull);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REGS_ELEM) : "memory");
+    const int wg = (warp - 4) / 4;
+    const int quarter = warp % 4;
+    const int row = quarter * 32 + lane;  // query row of this thread
+    const uint32_t lane_bits = (uint32_t)(quarter * 32) << 16;
+    const int c0 = wg * 64;               // key columns of this warpgroup
+    const float sl2 = p.scale_log2;
+    const int64_t grow = row_index(p, bh, qt, row < qt.valid ? row : 0);
+    const int64_t vrow = vec_index(p, bh, qt, row < qt.valid ? row : 0);
+    const float l2 = row < qt.valid ? p.l2[vrow] : 0.f;
+    const float dlt = row < qt.valid ? p.delta[vrow] : 0.f;
+    const uint64_t sl2x2 = ptx::f2_pack(sl2, sl2), nl2 = ptx::f2_pack(-l2, -l2), ndl = ptx::f2_pack(-dlt, -dlt);
+    bool ok = true;
+    for (int j = 0; j < p.tiles; ++j) {
+      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_SFULL), (uint32_t)(j & 1), G, abort_flag, kDevTimeoutSoftmax));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      uint32_t sr[64], dr[64];
+      ld64(tS + lane_bits + c0, sr);
+      ld64(tdP + lane_bits + c0, dr);
+      const int valid = tile_ref(p, j).valid - c0;  // key columns of this warpgroup that exist
+      if (valid < 64) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+      }
+      uint32_t dk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float x0, x1, y0, y1, d0, d1;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, nl2),
+                       x0, x1);
+        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])), ndl), y0,
+                       y1);
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), ptx::f2_pack(y0, y1)), d0, d1);
+        dk[c] = ptx::bf16x2(d0, d1);
+      }
+      ptx::tmem_st32(tS + lane_bits + c0, dk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(B_PFULL));
+    }
+    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
+    if (ok) {
+      ptx::tc_fence_after();
+      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst0) + grow * HD + c0, tdQ + lane_bits + c0, p.scale,
+                  row < qt.valid);
+    }
+  }
+  teardown(tmem, warp);
+}
+
+// =====================================================================
+// Delta = rowsum(dO * O) (fp32) and L2 = lse * log2(e): 16 threads per row
+// of 128 bf16, 16-byte loads, shuffle reduction over the 16 lanes.
+// =====================================================================
+__global__ void __launch_bounds__(256) usp_bwd_prep_kernel(const __nv_bfloat16* __restrict__ out,
+                                                           const __nv_bfloat16* __restrict__ dout,
+                                                           const float* __restrict__ lse, float* __restrict__ delta,
+                                                           float* __restrict__ l2, int64_t rows, int64_t Ns,
+                                                           int64_t Ns_pad) {
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t row = gt / 16;
+  const int part = (int)(gt % 16);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(out + row * HD) + part);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(dout + row * HD) + part);
+    const __nv_bfloat162* ha = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(ha[i]), y = __bfloat1622float2(hb[i]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) {
+    const int64_t v = (row / Ns) * Ns_pad + row % Ns;  // padded pitch for the tensor map
+    delta[v] = acc;
+    l2[v] = lse[row] * LOG2E;
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+bool map_stack_bf16(CUtensorMap* m, const void* base, int64_t Ns, int64_t BH, int64_t sp) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)HD, (cuuint64_t)Ns, (cuuint64_t)BH, (cuuint64_t)sp};
+  cuuint64_t strides[3] = {(cuuint64_t)HD * 2, (cuuint64_t)Ns * HD * 2, (cuuint64_t)BH * Ns * HD * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)BM, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// fp32 per-row vector [sp][BH][Ns] with row pitch Ns_pad; 128-row boxes.
+bool map_stack_f32(CUtensorMap* m, const void* base, int64_t Ns, int64_t Ns_pad, int64_t BH, int64_t sp) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)Ns, (cuuint64_t)BH, (cuuint64_t)sp};
+  cuuint64_t strides[2] = {(cuuint64_t)Ns_pad * 4, (cuuint64_t)BH * Ns_pad * 4};
+  cuuint32_t box[3] = {(cuuint32_t)BM, 1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(usp_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(usp_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int64_t rows = a.BH * a.sp * a.Ns;
+  const int64_t Ns_pad = (a.Ns + 3) / 4 * 4;
+  usp_bwd_prep_kernel<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, stream>>>(
+      (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, a.delta, a.l2, rows, a.Ns, Ns_pad);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mq, mk, mv, mdo, ml2, mdl;
+  if (!map_stack_bf16(&mq, a.q, a.Ns, a.BH, a.sp) || !map_stack_bf16(&mk, a.k, a.Ns, a.BH, a.sp) ||
+      !map_stack_bf16(&mv, a.v, a.Ns, a.BH, a.sp) || !map_stack_bf16(&mdo, a.dout, a.Ns, a.BH, a.sp) ||
+      !map_stack_f32(&ml2, a.l2, a.Ns, Ns_pad, a.BH, a.sp) || !map_stack_f32(&mdl, a.delta, a.Ns, Ns_pad, a.BH, a.sp))
+    return cudaErrorInvalidValue;
+  BwdParams p{};
+  p.l2 = a.l2;
+  p.delta = a.delta;
+  p.BH = a.BH;
+  p.Ns = a.Ns;
+  p.Ns_pad = Ns_pad;
+  p.tiles_per_seg = (int)((a.Ns + BM - 1) / BM);
+  p.tiles = (int)(p.tiles_per_seg * a.sp);
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * LOG2E;
+  p.guard = g;
+  dim3 grid((unsigned)p.tiles, (unsigned)a.BH, 1);
+  p.dst0 = a.dk;
+  p.dst1 = a.dv;
+  usp_bwd_dkdv_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mdo, ml2, mdl, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  p.dst0 = a.dq;
+  p.dst1 = nullptr;
+  usp_bwd_dq_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace usp

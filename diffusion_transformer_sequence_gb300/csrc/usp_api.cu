@@ -84,6 +84,13 @@ int check_kernel(usp_dtype dt, int64_t D) {
   return USP_OK;
 }
 
+// Delta and lse*log2(e) per row, rows padded to a multiple of 4 per shard so
+// each (shard, head) row block starts 16-byte aligned (tensor-map pitch).
+size_t bwd_vec_bytes(int64_t B, int64_t H, int64_t N, int u, int r) {
+  const int64_t sp = (int64_t)u * r, Ns = N / sp;
+  return round_up((size_t)(sp * B * H * ((Ns + 3) / 4 * 4)) * 4);
+}
+
 struct FwdWorkspace {
   size_t xq, xk, xv, parts_o, parts_l, xo, xl, total;
 };
@@ -213,7 +220,7 @@ int usp_lse_merge(const void* outs, const float* lses, int R, void* out, float* 
 size_t usp_attention_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring,
                                      usp_dtype dtype, usp_mode mode, int backward) {
   if (check_dims(B, H, N, D, ulysses, ring) != USP_OK || check_kernel(dtype, D) != USP_OK) return 0;
-  if (backward) return 0;
+  if (backward) return 2 * bwd_vec_bytes(B, H, N, ulysses, ring);  // Delta and lse*log2(e)
   if (mode == USP_FUSED) return 0;
   return fwd_layout(B, H, N, D, ring, dtype).total;
 }
@@ -284,11 +291,43 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
                       const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N, int64_t D,
                       int ulysses, int ring, float scale, usp_dtype dtype, void* workspace, size_t workspace_bytes,
                       usp_stream_t stream) {
-  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)dq; (void)dk; (void)dv;
-  (void)workspace; (void)workspace_bytes; (void)stream; (void)scale;
   int st = check_dims(B, H, N, D, ulysses, ring);
   if (st != USP_OK) return st;
-  return USP_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  st = check_kernel(dtype, D);
+  if (st != USP_OK) return st;
+  if (B * H * N == 0) return USP_OK;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return USP_ERR_INVALID_ARG;
+  if (dtype == USP_BF16 && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) &&
+                             aligned(dout, 16) && aligned(dq, 16) && aligned(dk, 16) && aligned(dv, 16)))
+    return USP_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return USP_ERR_INVALID_ARG;
+  const size_t lb = bwd_vec_bytes(B, H, N, ulysses, ring);
+  if (!workspace || workspace_bytes < 2 * lb) return USP_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return USP_ERR_INVALID_ARG;
+  const int64_t sp = (int64_t)ulysses * ring, Ns = N / sp;
+  if (B * H > 65535 || (Ns + 127) / 128 * sp > 2147483647LL) return USP_ERR_UNSUPPORTED;
+  float* delta = static_cast<float*>(workspace);
+  float* l2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + lb);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if (dtype == USP_F32) {
+    e = launch_attn_f32_bwd((const float*)q, (const float*)k, (const float*)v, (const float*)out, lse,
+                            (const float*)dout, (float*)dq, (float*)dk, (float*)dv, delta, B * H, sp, Ns, (int)D,
+                            scale, s);
+  } else {
+    Guard g;
+    st = guard(&g);
+    if (st != USP_OK) return st;
+    TcBwdArgs a{};
+    a.q = q; a.k = k; a.v = v; a.out = out; a.dout = dout; a.lse = lse;
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    a.delta = delta; a.l2 = l2;
+    a.BH = B * H; a.sp = sp; a.Ns = Ns;
+    a.scale = scale;
+    e = launch_attn_tc_bwd(a, g, s);
+  }
+  return e == cudaSuccess ? USP_OK : cuda_fail(e);
 }
 
 int usp_device_status(usp_stream_t stream) {

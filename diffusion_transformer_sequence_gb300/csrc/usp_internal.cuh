@@ -67,9 +67,24 @@ struct TcAttnArgs {
 };
 cudaError_t launch_attn_tc_fwd(const TcAttnArgs& a, const Guard& g, cudaStream_t stream);
 
-// backward helpers
-cudaError_t launch_bwd_delta(const void* out, const void* dout, float* delta, int64_t rows, int D,
-                             int dtype, cudaStream_t stream);
+// bf16 tcgen05 backward over token-sharded stacks (D = 128): prep (Delta,
+// lse*log2e into workspace), dK/dV kernel, dQ kernel.
+struct TcBwdArgs {
+  const void *q, *k, *v, *out, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  float* delta;  // workspace [sp][BH][Ns]
+  float* l2;     // workspace [sp][BH][Ns]
+  int64_t BH, sp, Ns;
+  float scale;
+};
+cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t stream);
+
+// fp32 backward on the FP32 pipes over token-sharded stacks.
+cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, const float* out,
+                                const float* lse, const float* dout, float* dq, float* dk, float* dv,
+                                float* delta, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
+                                cudaStream_t stream);
 
 Guard current_guard();  // the guard for the current device (error word + limits)
 

@@ -1,0 +1,110 @@
+"""GPU parity of usp_attention_bwd against the oracle, through the C ABI.
+
+Small problems: every row of dq, dk, dv against oracle.attention_bwd, with the
+backward fed the oracle's own forward (out rounded to the input dtype, lse to
+fp32, both on the test side).  Wan shapes (u8 x r4, N = 32768): the GPU
+forward feeds the GPU backward; the oracle recomputes everything from q, k,
+v, dO and checks 4096 sampled query rows (dq) and 4096 sampled key rows (dk,
+dv) on four heads, two of them on either side of a Ulysses head-group
+boundary.  Tolerance (no bound is stated for gradients): per tensor
+max|err| / max|ref| <= 2e-2 in bf16, max|err| <= 1e-5 in fp32."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import pool
+from diffusion_transformer_sequence_gb300 import workloads as wl
+from tests.helpers import BF16_GRAD_REL, F32_GRAD_ATOL, Canary, ensure_built, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    assert torch.cuda.is_available()
+
+
+def _usp():
+    import diffusion_transformer_sequence_gb300 as usp
+    return usp
+
+
+def _check_grad(got, ref, dtype, what):
+    g = f64(got)
+    assert np.isfinite(g).all(), f"{what}: non-finite"
+    err = np.abs(g - ref).max()
+    if dtype == "f32":
+        assert err <= F32_GRAD_ATOL, f"{what}: max err {err:.3e}"
+    else:
+        rel = err / max(np.abs(ref).max(), 1e-30)
+        assert rel <= BF16_GRAD_REL, f"{what}: rel err {rel:.3e} (abs {err:.3e})"
+
+
+SMALL = [
+    ("bf16", 1, 2, 512, 2, 2),
+    ("bf16", 2, 6, 960, 3, 2),     # ragged tiles in every shard
+    ("bf16", 1, 8, 800, 8, 1),     # shards shorter than one tile
+    ("bf16", 1, 2, 384, 1, 1),
+    ("bf16", 1, 2, 1000, 2, 4),    # Ns = 125: row pitch padding of the per-row vectors
+    ("f32", 1, 4, 96, 2, 3),
+    ("f32", 2, 2, 50, 1, 5),
+]
+
+
+@pytest.mark.parametrize("dtype,B,H,N,u,r", SMALL)
+def test_bwd_small_full_rows(dtype, B, H, N, u, r):
+    usp = _usp()
+    D = 128 if dtype == "bf16" else 32
+    w = wl.custom("bwd", dtype, B, H, N, D, u, r, seed=N + 7 * H, backward=True)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "dout"))
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v), w.scale)
+    dq_r, dk_r, dv_r = oracle.attention_bwd(f64(q), f64(k), f64(v), o_ref, l_ref, f64(do), w.scale)
+    o_in = torch.from_numpy(o_ref).to(w.torch_dtype)
+    l_in = torch.from_numpy(l_ref).float()
+    st = lambda t: wl.to_token_stack(t, u, r).cuda()
+    cans = [Canary(w.stack_shape, w.torch_dtype) for _ in range(3)]
+    dq, dk, dv = (c.view for c in cans)
+    L = usp.lib()
+    from diffusion_transformer_sequence_gb300 import _lib
+    need = usp.workspace_bytes(B, H, N, D, u, r, w.torch_dtype, backward=True)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = [st(q), st(k), st(v), st(o_in), st(l_in), st(do)]
+    rc = L.usp_attention_bwd(*[a.data_ptr() for a in args], dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+                             u, r, w.scale, _lib.USP_F32 if dtype == "f32" else _lib.USP_BF16, ws.data_ptr(), need,
+                             torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    assert usp.device_status() == 0
+    for c in cans:
+        c.check()
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        _check_grad(wl.from_token_stack(got.cpu()), ref, dtype, f"{name} {dtype} B{B} H{H} N{N} u{u} r{r}")
+
+
+def test_bwd_wan_shapes_sampled():
+    """Wan shapes (B1 H40 N32768 D128, u8 x r4), forward + backward on the GPU."""
+    usp = _usp()
+    w = wl.WORKLOADS["wan_s32k"]
+    inp = wl.make_inputs(w)
+    st = {n: wl.to_token_stack(t, w.ulysses, w.ring).cuda() for n, t in inp.items()}
+    o, l = usp.attention_fwd(st["q"], st["k"], st["v"], w.ulysses, w.ring, w.scale, mode="fused")
+    dq, dk, dv = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], w.ulysses, w.ring, w.scale)
+    assert usp.device_status() == 0
+    dq2, dk2, dv2 = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], w.ulysses, w.ring, w.scale)
+    for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):    # deterministic: no atomics anywhere
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    heads = [0, 4, 5, 39]   # Hu = 5: heads 4 | 5 sit on either side of a Ulysses group boundary
+    qrows = wl.sample_rows(w, 4096)
+    g = torch.Generator().manual_seed(w.row_seed + 1)
+    krows = torch.unique(torch.cat([qrows[::2], torch.randperm(w.N, generator=g)[:2048]]))
+    flat = {n: inp[n].reshape(w.B * w.H, w.N, w.D) for n in inp}
+    sel = lambda t, rows: wl.from_token_stack(t).reshape(w.B * w.H, w.N, w.D)[heads][:, rows.cuda()]
+    g_dq, g_dk, g_dv = sel(dq, qrows), sel(dk, krows), sel(dv, krows)
+    f = lambda n: flat[n].float().numpy()
+    r_dq, r_dk, r_dv = pool.sampled_backward(f("q"), f("k"), f("v"), f("dout"), w.scale, heads, qrows.numpy(),
+                                             krows.numpy())
+    _check_grad(g_dq, r_dq, "bf16", "wan dq")
+    _check_grad(g_dk, r_dk, "bf16", "wan dk")
+    _check_grad(g_dv, r_dv, "bf16", "wan dv")
