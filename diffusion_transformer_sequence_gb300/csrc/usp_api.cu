@@ -14,7 +14,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/usp.h"
+#include "usp.h"
 #include "usp_internal.cuh"
 
 namespace usp {

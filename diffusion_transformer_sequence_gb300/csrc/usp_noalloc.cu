@@ -24,7 +24,7 @@
 // must be serialised by the caller.
 #include <mutex>
 
-#include "../../include/usp.h"
+#include "usp.h"
 #include "usp_internal.cuh"
 
 namespace usp {
