@@ -15,16 +15,14 @@
 //
 //   usp_bwd_prep_kernel   Delta = rowsum(dO * O) and L2 = lse * log2(e), fp32
 //   usp_bwd_dkdv_kernel   one CTA per (head, 128-key tile); loops over every
-//                         64-query sub-tile: S^T = K Q^T, dP^T = V dO^T (TMEM),
+//                         128-query tile: S^T = K Q^T, dP^T = V dO^T (TMEM),
 //                         P^T, dS^T in registers -> bf16 back into TMEM,
 //                         dV += P^T dO, dK += dS^T Q (TMEM accumulators)
 //   usp_bwd_dq_kernel     one CTA per (head, 128-query tile); loops over every
-//                         64-key sub-tile: S = Q K^T, dP = dO V^T, dS -> TMEM,
+//                         128-key tile: S = Q K^T, dP = dO V^T, dS -> TMEM,
 //                         dQ += dS K
 // Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator + MMA issuer,
-// warps 4..11 two elementwise warpgroups, ping-ponging over two TMEM buffers
-// (a thread owns one TMEM lane = one row; each warpgroup writes its packed
-// bf16 results back inside the columns it has already read).
+// warps 4..11 two elementwise warpgroups splitting the columns of each tile.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -41,7 +39,6 @@ constexpr int TILE_BYTES = BM * HD * 2;
 constexpr int HALF_BYTES = TILE_BYTES / 2;
 constexpr int VEC_BYTES = BM * 4;  // 128 fp32 (L2 or Delta of one tile)
 constexpr int NUM_THREADS = 384;
-constexpr int STAGES = 2;
 constexpr int REGS_CTRL = 56;
 constexpr int REGS_ELEM = (NUM_THREADS * 168 - 128 * REGS_CTRL) / 256 / 8 * 8;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -82,32 +79,41 @@ __device__ __forceinline__ int64_t vec_index(const BwdParams& p, int64_t bh, con
   return ((int64_t)t.seg * p.BH + bh) * p.Ns_pad + t.row0 + r;
 }
 
-// Shared-memory layout (both kernels): two resident tiles A0, A1, then
-// STAGES x (two streamed tiles + two fp32 vectors), then barriers.
+// Shared memory (both kernels): two resident 128-row tiles A0, A1 (K and V
+// for dK/dV, Q and dO for dQ), STAGES x (two streamed 128-row tiles + two
+// fp32 vectors), then barriers.  Every GEMM is a 128 x 128 (x 128 or 64)
+// tcgen05.mma: narrower N would make the shared-memory operand fetch, not the
+// tensor core, the bound.
+constexpr int STAGES = 2;
 constexpr int OFF_A0 = 0;
 constexpr int OFF_A1 = TILE_BYTES;
 constexpr int OFF_STAGE = 2 * TILE_BYTES;
 constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * VEC_BYTES;
 constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-constexpr int B_RES = 0;                 // resident tiles loaded
-constexpr int B_FULL = 1;                // + stage
-constexpr int B_EMPTY = B_FULL + STAGES;  // + stage
-constexpr int B_SFULL = B_EMPTY + STAGES;  // + buffer
-constexpr int B_PFULL = B_SFULL + 2;       // + buffer
-constexpr int B_ODONE = B_PFULL + 2;
-constexpr int B_MMADONE = B_ODONE + 1;
-constexpr int NUM_BARS = B_MMADONE + 1;
+enum Bar : int {
+  B_RES = 0,                    // resident tiles landed
+  B_FULL = 1,                   // + stage
+  B_EMPTY = B_FULL + STAGES,    // + stage
+  B_SFULL = B_EMPTY + STAGES,   // S-like GEMM done
+  B_DPFULL,                     // dP-like GEMM done
+  B_PREADY,                     // dK/dV: P^T written to TMEM      | dQ: S read (free)
+  B_DSREADY,                    // dS written to TMEM (dK/dV: slot 0; dQ: + dS buffer, so a
+                                //   phase can never be completed twice before it is observed)
+  B_DPFREE = B_DSREADY + 2,     // dQ: dP read (free)
+  B_DQDONE,                     // dQ: + dS buffer, dQ GEMM that read it done
+  B_ODONE = B_DQDONE + 2,
+  B_MMADONE,
+  NUM_BARS
+};
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_SLOT + 8;
 constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint32_t stage_addr(uint32_t sbase, int s) { return sbase + OFF_STAGE + s * STAGE_BYTES; }
 
-// 64 columns per lane: two 32-column loads, one wait.
-__device__ __forceinline__ void ld64(uint32_t taddr, uint32_t* r) { ptx::tmem_ld64(taddr, r); }
-
-// Common prologue: barriers, TMEM, register split.  Returns the TMEM base.
-__device__ __forceinline__ uint32_t prologue(uint8_t* smem, uint32_t sbase, int warp, int lane, uint32_t pfull_count) {
+// Common prologue: barriers and TMEM.  Returns the TMEM base.
+__device__ __forceinline__ uint32_t prologue(uint8_t* smem, uint32_t sbase, int warp) {
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_RES), 1);
@@ -115,10 +121,14 @@ __device__ __forceinline__ uint32_t prologue(uint8_t* smem, uint32_t sbase, int 
       ptx::mbar_init(bar(B_FULL + s), 1);
       ptx::mbar_init(bar(B_EMPTY + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(bar(B_SFULL + b), 1);
-      ptx::mbar_init(bar(B_PFULL + b), pfull_count);
-    }
+    ptx::mbar_init(bar(B_SFULL), 1);
+    ptx::mbar_init(bar(B_DPFULL), 1);
+    ptx::mbar_init(bar(B_PREADY), 256);
+    ptx::mbar_init(bar(B_DSREADY), 256);
+    ptx::mbar_init(bar(B_DSREADY + 1), 256);
+    ptx::mbar_init(bar(B_DPFREE), 256);
+    ptx::mbar_init(bar(B_DQDONE), 1);
+    ptx::mbar_init(bar(B_DQDONE + 1), 1);
     ptx::mbar_init(bar(B_ODONE), 1);
     ptx::mbar_init(bar(B_MMADONE), 1);
     *reinterpret_cast<volatile int*>(smem + OFF_ABORT) = 0;
@@ -163,29 +173,29 @@ __device__ __forceinline__ void store_row64(__nv_bfloat16* dst, uint32_t taddr, 
   }
 }
 
-// Sub-tile pipeline shared by both kernels.  The streamed 128-row tiles are
-// processed as 64-row sub-tiles u = 0, 1, 2, ... through two TMEM buffers:
-// buffer b = u % 2 holds S-like [0,64) and dP-like [64,128) columns of
-// sub-tile u, elementwise warpgroup b handles every sub-tile of its parity
-// (so warpgroup b always owns half b of each 128-row tile), and the MMA issue
-// order S(0); S(1), G(0); S(2), G(1); ... lets the elementwise work on
-// sub-tile u overlap the tensor core's G(u-1) and S(u+1), where G is the
-// gradient GEMM(s) that consume sub-tile u's bf16 results.
-constexpr int SUB = 64;
-constexpr int SUB_BYTES = SUB * 128;  // 64 rows of one 128-byte swizzled half
-
-// K-major operand descriptor of k-step kk (16 of the 128 head-dim columns)
-// of a 64- or 128-row tile at `base` (sub-tile offset already added).
+// K-major operand descriptor of k-step kk (16 of the 128 head-dim columns).
 __device__ __forceinline__ uint64_t kmajor_step(uint64_t d0, int kk) {
   return d0 + (uint64_t)((((kk / 4) * HALF_BYTES) + (kk % 4) * 32) >> 4);
 }
+// A-operand (packed bf16) column of k-step kk when warpgroup 0 wrote rows
+// [0,64) at columns [0,32) and warpgroup 1 wrote [64,128) at [64,96).
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 : 64 + (kk - 4) * 8; }
+
+// Elementwise warps split every phase in two so the tensor core always has an
+// independent 128-wide GEMM queued behind the one the warps are waiting for:
+//   dK/dV per query tile i:  S^T(i) dP^T(i) | dV(i) S^T(i+1) | dK(i) dP^T(i+1) ...
+//     the warps compute P^T(i) while dP^T(i) runs, dS^T(i) while dV(i) and
+//     S^T(i+1) run;
+//   dQ per key tile j:  S(j+1) dP(j+1) dQ(j) ...  the warps release S(j) and
+//     dP(j) as soon as they have read them and write dS(j) into one of two
+//     spare TMEM buffers.
+// (a thread owns one TMEM lane = one row; warpgroup w owns columns
+// [64w, 64w+64) and writes its packed bf16 results inside columns it has read)
 
 // =====================================================================
-// dK, dV: one CTA per (head, 128-key tile); resident K (A0), V (A1); streamed
-// Q, dO, L2, Delta per 128-query tile, consumed as two 64-query sub-tiles.
-// TMEM: buffer b: S^T [128b, 128b+64), dP^T [128b+64, 128b+128);
-//       dV [256,384), dK [384,512).  P^T / dS^T (bf16) overwrite the first 32
-//       columns of S^T / dP^T of their buffer.
+// dK, dV: one CTA per (head, 128-key tile); resident K (A0), V (A1);
+// streamed Q, dO, L2, Delta per 128-query tile.
+// TMEM: S^T [0,128)  dP^T [128,256)  dV [256,384)  dK [384,512).
 // =====================================================================
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     usp_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -201,9 +211,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int64_t bh = blockIdx.y;
   const TileRef kt = tile_ref(p, blockIdx.x);
   const Guard& G = p.guard;
-  const uint32_t tmem = prologue(smem, sbase, warp, lane, 128);
-  const uint32_t tdV = tmem + 256, tdK = tmem + 384;
-  const int U = 2 * p.tiles;  // 64-query sub-tiles
+  const uint32_t tmem = prologue(smem, sbase, warp);
+  const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
+  const int T = p.tiles;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REGS_CTRL) : "memory");
@@ -213,7 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       load_tile(&tm_k, sbase + OFF_A0, bar(B_RES), bh, kt);
       load_tile(&tm_v, sbase + OFF_A1, bar(B_RES), bh, kt);
       int issued = 0;
-      for (int i = 0; i < p.tiles; ++i) {
+      for (int i = 0; i < T; ++i) {
         const int s = i % STAGES;
         const uint32_t ph = (uint32_t)((i / STAGES) & 1);
         if (!ptx::mbar_wait(bar(B_EMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
@@ -231,52 +241,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (i >= 0) ptx::mbar_drain(bar(B_FULL + i % STAGES), (uint32_t)((i / STAGES) & 1), 200000000ull);
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      constexpr uint32_t ID_S = ptx::idesc_bf16_f32(BM, SUB, 0, 0);  // S^T, dP^T: keys x 64 queries
-      constexpr uint32_t ID_G = ptx::idesc_bf16_f32(BM, HD, 0, 1);   // dV, dK: B = dO / Q, N-major
+      constexpr uint32_t ID_S = ptx::idesc_bf16_f32(BM, BM, 0, 0);  // S^T, dP^T
+      constexpr uint32_t ID_G = ptx::idesc_bf16_f32(BM, HD, 0, 1);  // dV, dK (B = dO / Q, N-major)
       const uint64_t dK0 = ptx::smem_desc_sw128(sbase + OFF_A0, 16, 1024);
       const uint64_t dV0 = ptx::smem_desc_sw128(sbase + OFF_A1, 16, 1024);
-      bool ok = ptx::mbar_wait(bar(B_RES), 0, G, abort_flag, kDevTimeoutMma);
-      auto issue_s = [&](int u) -> bool {
-        const int tile = u >> 1, half = u & 1, s = tile % STAGES, b = u & 1;
-        if (half == 0) {
-          if (!ptx::mbar_wait(bar(B_FULL + s), (uint32_t)((tile / STAGES) & 1), G, abort_flag, kDevTimeoutMma))
-            return false;
-          ptx::tc_fence_after();
-        }
-        const uint32_t st = stage_addr(sbase, s) + half * SUB_BYTES;
-        const uint64_t dq = ptx::launder(ptx::smem_desc_sw128(st, 16, 1024));
-        const uint64_t ddo = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, 16, 1024));
-        const uint32_t tS = tmem + 128 * b;
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tS, kmajor_step(dK0, kk), kmajor_step(dq, kk), ID_S, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tS + 64, kmajor_step(dV0, kk), kmajor_step(ddo, kk), ID_S, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(B_SFULL + b));
-        return true;
-      };
-      auto issue_g = [&](int u) -> bool {
-        const int tile = u >> 1, half = u & 1, s = tile % STAGES, b = u & 1;
-        if (!ptx::mbar_wait(bar(B_PFULL + b), (uint32_t)((u >> 1) & 1), G, abort_flag, kDevTimeoutMma)) return false;
+      auto wait = [&](int b, uint32_t ph) { return ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutMma); };
+      auto issue_st = [&](int i) -> bool {  // S^T(i) = K Q_i^T
+        const int s = i % STAGES;
+        if (!wait(B_FULL + s, (uint32_t)((i / STAGES) & 1))) return false;
         ptx::tc_fence_after();
-        const uint32_t st = stage_addr(sbase, s) + half * SUB_BYTES;
-        const uint64_t bdo = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, HALF_BYTES, 1024));
-        const uint64_t bq = ptx::launder(ptx::smem_desc_sw128(st, HALF_BYTES, 1024));
-        const uint32_t tS = tmem + 128 * b;
+        const uint64_t dq = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, s), 16, 1024));
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk)  // dV += P^T dO (K = the sub-tile's queries)
-          ptx::mma_ts(tdV, tS + kk * 8, bdo + (uint64_t)((kk * 2048) >> 4), ID_G, (u > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk)  // dK += dS^T Q
-          ptx::mma_ts(tdK, tS + 64 + kk * 8, bq + (uint64_t)((kk * 2048) >> 4), ID_G, (u > 0 || kk > 0) ? 1u : 0u);
-        if (half == 1) ptx::mma_commit(bar(B_EMPTY + s));
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tSt, kmajor_step(dK0, kk), kmajor_step(dq, kk), ID_S, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(B_SFULL));
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int u = 0; ok && u < U; ++u) {
-        if (u + 1 < U && !(ok = issue_s(u + 1))) break;
-        ok = issue_g(u);
+      auto issue_dpt = [&](int i) {  // dP^T(i) = V dO_i^T (stage already waited for by S^T(i))
+        const uint64_t ddo = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, i % STAGES) + TILE_BYTES, 16, 1024));
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          ptx::mma_ss(tdPt, kmajor_step(dV0, kk), kmajor_step(ddo, kk), ID_S, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(B_DPFULL));
+      };
+      bool ok = wait(B_RES, 0);
+      if (ok) ok = issue_st(0);
+      if (ok) issue_dpt(0);
+      for (int i = 0; ok && i < T; ++i) {
+        const uint32_t st = stage_addr(sbase, i % STAGES);
+        if (!(ok = wait(B_PREADY, (uint32_t)(i & 1)))) break;
+        ptx::tc_fence_after();
+        const uint64_t bdo = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, HALF_BYTES, 1024));
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dV += P^T dO (K = queries)
+          ptx::mma_ts(tdV, tSt + packed_col(kk), bdo + (uint64_t)((kk * 2048) >> 4), ID_G, (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 1 < T && !(ok = issue_st(i + 1))) break;
+        if (!(ok = wait(B_DSREADY, (uint32_t)(i & 1)))) break;
+        ptx::tc_fence_after();
+        const uint64_t bq = ptx::launder(ptx::smem_desc_sw128(st, HALF_BYTES, 1024));
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dK += dS^T Q
+          ptx::mma_ts(tdK, tdPt + packed_col(kk), bq + (uint64_t)((kk * 2048) >> 4), ID_G, (i > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(B_EMPTY + i % STAGES));
+        if (i + 1 < T) issue_dpt(i + 1);
       }
       if (ok) ptx::mma_commit(bar(B_ODONE));
       ptx::mma_commit(bar(B_MMADONE));
@@ -285,66 +292,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REGS_ELEM) : "memory");
     // ------------------------------------------------------------ elementwise
-    const int wg = (warp - 4) / 4;        // buffer and tile half owned by this warpgroup
+    const int wg = (warp - 4) / 4;
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;  // key row of this thread
     const uint32_t lane_bits = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + 128 * wg;
+    const int c0 = wg * 64;               // query columns of this warpgroup
     const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2);
+    auto wait = [&](int b, uint32_t ph) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutSoftmax));
+    };
     bool ok = true;
-    for (int u = wg; u < U; u += 2) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_SFULL + wg), (uint32_t)((u >> 1) & 1), G, abort_flag,
-                                                  kDevTimeoutSoftmax));
-      if (!ok) break;
+    for (int i = 0; i < T; ++i) {
+      if (!(ok = wait(B_SFULL, (uint32_t)(i & 1)))) break;
       ptx::tc_fence_after();
-      const uint32_t st = stage_addr(sbase, (u >> 1) % STAGES);
-      const float* l2 = reinterpret_cast<const float*>(smem + (st - sbase) + 2 * TILE_BYTES) + wg * SUB;
-      const float* dl = reinterpret_cast<const float*>(smem + (st - sbase) + 2 * TILE_BYTES + VEC_BYTES) + wg * SUB;
-      uint32_t sr[64], dr[64];
-      ld64(tS, sr);
-      ld64(tS + 64, dr);
-      uint32_t pk[32], dk[32];
+      const uint32_t st = stage_addr(sbase, i % STAGES);
+      const float* l2 = reinterpret_cast<const float*>(smem + (st - sbase) + 2 * TILE_BYTES) + c0;
+      const float* dl = reinterpret_cast<const float*>(smem + (st - sbase) + 2 * TILE_BYTES + VEC_BYTES) + c0;
+      uint32_t r[64];
+      ptx::tmem_ld64(tSt + lane_bits + c0, r);
+      float pv[64];
+      uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        float x0, x1, y0, y1, d0, d1;
         const float2 lv = *reinterpret_cast<const float2*>(l2 + 2 * c);
-        const float2 dv = *reinterpret_cast<const float2*>(dl + 2 * c);
-        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2,
+        float x0, x1;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2x2,
                                    ptx::f2_pack(-lv.x, -lv.y)),
                        x0, x1);
-        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])),
-                                   ptx::f2_pack(-dv.x, -dv.y)),
-                       y0, y1);
-        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), ptx::f2_pack(y0, y1)), d0, d1);
-        pk[c] = ptx::bf16x2(p0, p1);
-        dk[c] = ptx::bf16x2(d0, d1);
+        pv[2 * c] = ptx::ex2(x0);
+        pv[2 * c + 1] = ptx::ex2(x1);
+        pk[c] = ptx::bf16x2(pv[2 * c], pv[2 * c + 1]);
       }
-      ptx::tmem_st32(tS, pk);
-      ptx::tmem_st32(tS + 64, dk);
+      ptx::tmem_st32(tSt + lane_bits + c0, pk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_PFULL + wg));
+      ptx::mbar_arrive(bar(B_PREADY));
+      if (!(ok = wait(B_DPFULL, (uint32_t)(i & 1)))) break;
+      ptx::tc_fence_after();
+      ptx::tmem_ld64(tdPt + lane_bits + c0, r);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float2 dv = *reinterpret_cast<const float2*>(dl + 2 * c);
+        float y0, y1, d0, d1;
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])),
+                                   ptx::f2_pack(-dv.x, -dv.y)),
+                       y0, y1);
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pv[2 * c], pv[2 * c + 1]), ptx::f2_pack(y0, y1)), d0, d1);
+        pk[c] = ptx::bf16x2(d0, d1);
+      }
+      ptx::tmem_st32(tdPt + lane_bits + c0, pk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(B_DSREADY));
     }
     // ------------------------------------------------------------ epilogue
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
     if (ok) {
       ptx::tc_fence_after();
-      const int c0 = wg * 64;  // head-dim columns stored by this warpgroup
       const bool store = row < kt.valid;
-      const int64_t r = row_index(p, bh, kt, store ? row : 0);
-      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst1) + r * HD + c0, tdV + lane_bits + c0, 1.f, store);
-      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst0) + r * HD + c0, tdK + lane_bits + c0, p.scale, store);
+      const int64_t rr = row_index(p, bh, kt, store ? row : 0);
+      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst1) + rr * HD + c0, tdV + lane_bits + c0, 1.f, store);
+      store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst0) + rr * HD + c0, tdK + lane_bits + c0, p.scale, store);
     }
   }
   teardown(tmem, warp);
 }
 
 // =====================================================================
-// dQ: one CTA per (head, 128-query tile); resident Q (A0), dO (A1); streamed
-// K, V per 128-key tile, consumed as two 64-key sub-tiles.
-// TMEM: buffer b: S [128b, 128b+64), dP [128b+64, 128b+128); dQ [256,384).
-// dS (bf16) overwrites the first 32 columns of S of its buffer.
+// dQ: one CTA per (head, 128-query tile); resident Q (A0), dO (A1);
+// streamed K, V per 128-key tile.
+// TMEM: S [0,128)  dP [128,256)  dQ [256,384)  dS buffers [384,448) [448,512).
 // =====================================================================
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     usp_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -359,9 +376,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int64_t bh = blockIdx.y;
   const TileRef qt = tile_ref(p, blockIdx.x);
   const Guard& G = p.guard;
-  const uint32_t tmem = prologue(smem, sbase, warp, lane, 128);
-  const uint32_t tdQ = tmem + 256;
-  const int U = 2 * p.tiles;  // 64-key sub-tiles
+  const uint32_t tmem = prologue(smem, sbase, warp);
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384;
+  const int T = p.tiles;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REGS_CTRL) : "memory");
@@ -370,7 +387,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       load_tile(&tm_q, sbase + OFF_A0, bar(B_RES), bh, qt);
       load_tile(&tm_do, sbase + OFF_A1, bar(B_RES), bh, qt);
       int issued = 0;
-      for (int j = 0; j < p.tiles; ++j) {
+      for (int j = 0; j < T; ++j) {
         const int s = j % STAGES;
         const uint32_t ph = (uint32_t)((j / STAGES) & 1);
         if (!ptx::mbar_wait(bar(B_EMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
@@ -385,48 +402,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = issued - STAGES; j < issued; ++j)
         if (j >= 0) ptx::mbar_drain(bar(B_FULL + j % STAGES), (uint32_t)((j / STAGES) & 1), 200000000ull);
     } else if (warp == 1 && lane == 0) {
-      constexpr uint32_t ID_S = ptx::idesc_bf16_f32(BM, SUB, 0, 0);  // S, dP: queries x 64 keys
-      constexpr uint32_t ID_G = ptx::idesc_bf16_f32(BM, HD, 0, 1);   // dQ: B = K, N-major
+      constexpr uint32_t ID_S = ptx::idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
+      constexpr uint32_t ID_G = ptx::idesc_bf16_f32(BM, HD, 0, 1);  // dQ (B = K, N-major)
       const uint64_t dQ0 = ptx::smem_desc_sw128(sbase + OFF_A0, 16, 1024);
       const uint64_t dO0 = ptx::smem_desc_sw128(sbase + OFF_A1, 16, 1024);
-      bool ok = ptx::mbar_wait(bar(B_RES), 0, G, abort_flag, kDevTimeoutMma);
-      auto issue_s = [&](int u) -> bool {
-        const int tile = u >> 1, half = u & 1, s = tile % STAGES, b = u & 1;
-        if (half == 0) {
-          if (!ptx::mbar_wait(bar(B_FULL + s), (uint32_t)((tile / STAGES) & 1), G, abort_flag, kDevTimeoutMma))
-            return false;
-          ptx::tc_fence_after();
-        }
-        const uint32_t st = stage_addr(sbase, s) + half * SUB_BYTES;
-        const uint64_t dk = ptx::launder(ptx::smem_desc_sw128(st, 16, 1024));
-        const uint64_t dv = ptx::launder(ptx::smem_desc_sw128(st + TILE_BYTES, 16, 1024));
-        const uint32_t tS = tmem + 128 * b;
+      auto wait = [&](int b, uint32_t ph) { return ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutMma); };
+      auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T
+        const int s = j % STAGES;
+        if (!wait(B_FULL + s, (uint32_t)((j / STAGES) & 1))) return false;
+        ptx::tc_fence_after();
+        const uint64_t dk = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, s), 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           ptx::mma_ss(tS, kmajor_step(dQ0, kk), kmajor_step(dk, kk), ID_S, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(B_SFULL));
+        return true;
+      };
+      auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T
+        const uint64_t dv = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, j % STAGES) + TILE_BYTES, 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tS + 64, kmajor_step(dO0, kk), kmajor_step(dv, kk), ID_S, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(B_SFULL + b));
-        return true;
+          ptx::mma_ss(tdP, kmajor_step(dO0, kk), kmajor_step(dv, kk), ID_S, kk > 0 ? 1u : 0u);
+        ptx::mma_commit(bar(B_DPFULL));
       };
-      auto issue_g = [&](int u) -> bool {
-        const int tile = u >> 1, half = u & 1, s = tile % STAGES, b = u & 1;
-        if (!ptx::mbar_wait(bar(B_PFULL + b), (uint32_t)((u >> 1) & 1), G, abort_flag, kDevTimeoutMma)) return false;
-        ptx::tc_fence_after();
-        const uint32_t st = stage_addr(sbase, s) + half * SUB_BYTES;
-        const uint64_t bk = ptx::launder(ptx::smem_desc_sw128(st, HALF_BYTES, 1024));
-        const uint32_t tS = tmem + 128 * b;
-#pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk)  // dQ += dS K (K = the sub-tile's keys)
-          ptx::mma_ts(tdQ, tS + kk * 8, bk + (uint64_t)((kk * 2048) >> 4), ID_G, (u > 0 || kk > 0) ? 1u : 0u);
-        if (half == 1) ptx::mma_commit(bar(B_EMPTY + s));
-        return true;
-      };
+      bool ok = wait(B_RES, 0);
       if (ok) ok = issue_s(0);
-      for (int u = 0; ok && u < U; ++u) {
-        if (u + 1 < U && !(ok = issue_s(u + 1))) break;
-        ok = issue_g(u);
+      if (ok) issue_dp(0);
+      for (int j = 0; ok && j < T; ++j) {
+        if (j + 1 < T) {
+          if (!(ok = wait(B_PREADY, (uint32_t)(j & 1)))) break;   // S(j) read by the warps
+          if (!(ok = issue_s(j + 1))) break;
+          if (!(ok = wait(B_DPFREE, (uint32_t)(j & 1)))) break;   // dP(j) read by the warps
+          issue_dp(j + 1);
+        }
+        if (!(ok = wait(B_DSREADY + (j & 1), (uint32_t)((j >> 1) & 1)))) break;
+        ptx::tc_fence_after();
+        const uint64_t bk = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, j % STAGES), HALF_BYTES, 1024));
+        const uint32_t ds = ptx::launder(tdS + 64 * (j & 1));
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)  // dQ += dS K (K = keys)
+          ptx::mma_ts(tdQ, ds + kk * 8, bk + (uint64_t)((kk * 2048) >> 4), ID_G, (j > 0 || kk > 0) ? 1u : 0u);
+        ptx::mma_commit(bar(B_EMPTY + j % STAGES));
+        ptx::mma_commit(bar(B_DQDONE + (j & 1)));
       }
       if (ok) ptx::mma_commit(bar(B_ODONE));
       ptx::mma_commit(bar(B_MMADONE));
@@ -438,49 +455,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;  // query row of this thread
     const uint32_t lane_bits = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_bits + 128 * wg;
+    const int c0 = wg * 64;               // key columns of this warpgroup
     const int64_t grow = row_index(p, bh, qt, row < qt.valid ? row : 0);
     const int64_t vrow = vec_index(p, bh, qt, row < qt.valid ? row : 0);
     const float l2 = row < qt.valid ? p.l2[vrow] : 0.f;
     const float dlt = row < qt.valid ? p.delta[vrow] : 0.f;
     const uint64_t sl2x2 = ptx::f2_pack(p.scale_log2, p.scale_log2), nl2 = ptx::f2_pack(-l2, -l2),
                    ndl = ptx::f2_pack(-dlt, -dlt);
+    auto wait = [&](int b, uint32_t ph) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutSoftmax));
+    };
     bool ok = true;
-    for (int u = wg; u < U; u += 2) {
-      ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_SFULL + wg), (uint32_t)((u >> 1) & 1), G, abort_flag,
-                                                  kDevTimeoutSoftmax));
-      if (!ok) break;
+    for (int j = 0; j < T; ++j) {
+      if (!(ok = wait(B_SFULL, (uint32_t)(j & 1)))) break;
       ptx::tc_fence_after();
-      uint32_t sr[64], dr[64];
-      ld64(tS, sr);
-      ld64(tS + 64, dr);
-      const int valid = tile_ref(p, u >> 1).valid - wg * SUB;  // keys of this sub-tile that exist
-      if (valid < SUB) {
+      uint32_t r[64];
+      ptx::tmem_ld64(tS + lane_bits + c0, r);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(B_PREADY));     // S(j) may now be overwritten
+      const int valid = tile_ref(p, j).valid - c0;  // key columns of this warpgroup that exist
+      if (valid < 64) {
 #pragma unroll
-        for (int c = 0; c < SUB; ++c)
-          if (c >= valid) sr[c] = __float_as_uint(-INFINITY);
+        for (int c = 0; c < 64; ++c)
+          if (c >= valid) r[c] = __float_as_uint(-INFINITY);
       }
-      uint32_t dk[32];
+      float pv[64];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        float x0, x1, y0, y1, d0, d1;
-        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), sl2x2, nl2),
+        float x0, x1;
+        ptx::f2_unpack(ptx::f2_fma(ptx::f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2x2, nl2),
                        x0, x1);
-        const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])), ndl), y0,
-                       y1);
-        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(p0, p1), ptx::f2_pack(y0, y1)), d0, d1);
-        dk[c] = ptx::bf16x2(d0, d1);
+        pv[2 * c] = ptx::ex2(x0);
+        pv[2 * c + 1] = ptx::ex2(x1);
       }
-      ptx::tmem_st32(tS, dk);
+      if (!(ok = wait(B_DPFULL, (uint32_t)(j & 1)))) break;
+      ptx::tc_fence_after();
+      ptx::tmem_ld64(tdP + lane_bits + c0, r);
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(B_DPFREE));     // dP(j) may now be overwritten
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float y0, y1, d0, d1;
+        ptx::f2_unpack(ptx::f2_add(ptx::f2_pack(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), ndl), y0,
+                       y1);
+        ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pv[2 * c], pv[2 * c + 1]), ptx::f2_pack(y0, y1)), d0, d1);
+        pk[c] = ptx::bf16x2(d0, d1);
+      }
+      // dS(j) goes to buffer j % 2 once the dQ GEMM of tile j - 2 has read it
+      if (j >= 2 && !(ok = wait(B_DQDONE + (j & 1), (uint32_t)(((j - 2) >> 1) & 1)))) break;
+      ptx::tc_fence_after();
+      ptx::tmem_st32(tdS + lane_bits + 64 * (j & 1) + 32 * wg, pk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_PFULL + wg));
+      ptx::mbar_arrive(bar(B_DSREADY + (j & 1)));
     }
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
     if (ok) {
       ptx::tc_fence_after();
-      const int c0 = wg * 64;
       store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst0) + grow * HD + c0, tdQ + lane_bits + c0, p.scale,
                   row < qt.valid);
     }
