@@ -360,9 +360,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // =====================================================================
 // dQ: one CTA per (head, 128-query tile); resident Q (A0), dO (A1);
-// streamed K, V per 128-key tile.
+// streamed K through a 3-slot ring and V through a 2-slot ring (a K tile is
+// read by S(j) and, late, by dQ(j); a V tile only by dP(j), so the two are
+// released at different times and K needs the deeper ring to keep the next
+// loads in flight).
 // TMEM: S [0,128)  dP [128,256)  dQ [256,384)  dS buffers [384,448) [448,512).
 // =====================================================================
+constexpr int KSLOTS = 3, VSLOTS = 2;
+constexpr int DQ_OFF_K = 2 * TILE_BYTES;
+constexpr int DQ_OFF_V = DQ_OFF_K + KSLOTS * TILE_BYTES;
+constexpr int DQ_OFF_BAR = DQ_OFF_V + VSLOTS * TILE_BYTES;
+enum DqBar : int {
+  Q_RES = 0,
+  Q_KFULL = 1,
+  Q_KEMPTY = Q_KFULL + KSLOTS,
+  Q_VFULL = Q_KEMPTY + KSLOTS,
+  Q_VEMPTY = Q_VFULL + VSLOTS,
+  Q_SFULL = Q_VEMPTY + VSLOTS,
+  Q_DPFULL,
+  Q_SFREE,                  // S(j) read by the warps (256 arrivals)
+  Q_DPFREE,                 // dP(j) read (256)
+  Q_DSREADY,                // + dS buffer (256)
+  Q_DQDONE = Q_DSREADY + 2, // + dS buffer
+  Q_ODONE = Q_DQDONE + 2,
+  Q_MMADONE,
+  Q_NUM_BARS
+};
+constexpr int DQ_OFF_SLOT = DQ_OFF_BAR + Q_NUM_BARS * 8;
+constexpr int DQ_OFF_ABORT = DQ_OFF_SLOT + 8;
+constexpr int DQ_SMEM_BYTES = DQ_OFF_ABORT + 8 + 1024;
+static_assert(DQ_SMEM_BYTES <= 232448, "shared memory budget");
+
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     usp_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -370,84 +398,131 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
-  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
+  auto bar = [&](int i) -> uint32_t { return sbase + DQ_OFF_BAR + 8 * i; };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_ABORT);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int64_t bh = blockIdx.y;
   const TileRef qt = tile_ref(p, blockIdx.x);
   const Guard& G = p.guard;
-  const uint32_t tmem = prologue(smem, sbase, warp);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(Q_RES), 1);
+    for (int s = 0; s < KSLOTS; ++s) {
+      ptx::mbar_init(bar(Q_KFULL + s), 1);
+      ptx::mbar_init(bar(Q_KEMPTY + s), 1);
+    }
+    for (int s = 0; s < VSLOTS; ++s) {
+      ptx::mbar_init(bar(Q_VFULL + s), 1);
+      ptx::mbar_init(bar(Q_VEMPTY + s), 1);
+    }
+    ptx::mbar_init(bar(Q_SFULL), 1);
+    ptx::mbar_init(bar(Q_DPFULL), 1);
+    ptx::mbar_init(bar(Q_SFREE), 256);
+    ptx::mbar_init(bar(Q_DPFREE), 256);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(Q_DSREADY + b), 256);
+      ptx::mbar_init(bar(Q_DQDONE + b), 1);
+    }
+    ptx::mbar_init(bar(Q_ODONE), 1);
+    ptx::mbar_init(bar(Q_MMADONE), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(sbase + DQ_OFF_SLOT, 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem + DQ_OFF_SLOT);
   const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384;
   const int T = p.tiles;
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(REGS_CTRL) : "memory");
     if (warp == 0 && lane == 0) {
-      ptx::mbar_arrive_expect_tx(bar(B_RES), 2 * TILE_BYTES);
-      load_tile(&tm_q, sbase + OFF_A0, bar(B_RES), bh, qt);
-      load_tile(&tm_do, sbase + OFF_A1, bar(B_RES), bh, qt);
-      int issued = 0;
+      // ---------------------------------------------------------- producer
+      ptx::mbar_arrive_expect_tx(bar(Q_RES), 2 * TILE_BYTES);
+      load_tile(&tm_q, sbase + OFF_A0, bar(Q_RES), bh, qt);
+      load_tile(&tm_do, sbase + OFF_A1, bar(Q_RES), bh, qt);
+      int issued_k = 0, issued_v = 0;
+      // K runs ahead of V by up to one slot: issue in the order the MMAs consume
       for (int j = 0; j < T; ++j) {
-        const int s = j % STAGES;
-        const uint32_t ph = (uint32_t)((j / STAGES) & 1);
-        if (!ptx::mbar_wait(bar(B_EMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
         const TileRef kt = tile_ref(p, j);
-        const uint32_t st = stage_addr(sbase, s);
-        ptx::mbar_arrive_expect_tx(bar(B_FULL + s), 2 * TILE_BYTES);
-        load_tile(&tm_k, st, bar(B_FULL + s), bh, kt);
-        load_tile(&tm_v, st + TILE_BYTES, bar(B_FULL + s), bh, kt);
-        issued = j + 1;
+        const int sk = j % KSLOTS, sv = j % VSLOTS;
+        if (!ptx::mbar_wait(bar(Q_KEMPTY + sk), (uint32_t)(((j / KSLOTS) & 1) ^ 1), G, abort_flag,
+                            kDevTimeoutTmaProducer))
+          break;
+        ptx::mbar_arrive_expect_tx(bar(Q_KFULL + sk), TILE_BYTES);
+        load_tile(&tm_k, sbase + DQ_OFF_K + sk * TILE_BYTES, bar(Q_KFULL + sk), bh, kt);
+        issued_k = j + 1;
+        if (!ptx::mbar_wait(bar(Q_VEMPTY + sv), (uint32_t)(((j / VSLOTS) & 1) ^ 1), G, abort_flag,
+                            kDevTimeoutTmaProducer))
+          break;
+        ptx::mbar_arrive_expect_tx(bar(Q_VFULL + sv), TILE_BYTES);
+        load_tile(&tm_v, sbase + DQ_OFF_V + sv * TILE_BYTES, bar(Q_VFULL + sv), bh, kt);
+        issued_v = j + 1;
       }
-      ptx::mbar_drain(bar(B_RES), 0, 200000000ull);
-      for (int j = issued - STAGES; j < issued; ++j)
-        if (j >= 0) ptx::mbar_drain(bar(B_FULL + j % STAGES), (uint32_t)((j / STAGES) & 1), 200000000ull);
+      ptx::mbar_drain(bar(Q_RES), 0, 200000000ull);
+      for (int j = issued_k - KSLOTS; j < issued_k; ++j)
+        if (j >= 0) ptx::mbar_drain(bar(Q_KFULL + j % KSLOTS), (uint32_t)((j / KSLOTS) & 1), 200000000ull);
+      for (int j = issued_v - VSLOTS; j < issued_v; ++j)
+        if (j >= 0) ptx::mbar_drain(bar(Q_VFULL + j % VSLOTS), (uint32_t)((j / VSLOTS) & 1), 200000000ull);
     } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t ID_S = ptx::idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
       constexpr uint32_t ID_G = ptx::idesc_bf16_f32(BM, HD, 0, 1);  // dQ (B = K, N-major)
       const uint64_t dQ0 = ptx::smem_desc_sw128(sbase + OFF_A0, 16, 1024);
       const uint64_t dO0 = ptx::smem_desc_sw128(sbase + OFF_A1, 16, 1024);
       auto wait = [&](int b, uint32_t ph) { return ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutMma); };
       auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T
-        const int s = j % STAGES;
-        if (!wait(B_FULL + s, (uint32_t)((j / STAGES) & 1))) return false;
+        const int sk = j % KSLOTS;
+        if (!wait(Q_KFULL + sk, (uint32_t)((j / KSLOTS) & 1))) return false;
         ptx::tc_fence_after();
-        const uint64_t dk = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, s), 16, 1024));
+        const uint64_t dk = ptx::launder(ptx::smem_desc_sw128(sbase + DQ_OFF_K + sk * TILE_BYTES, 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           ptx::mma_ss(tS, kmajor_step(dQ0, kk), kmajor_step(dk, kk), ID_S, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(B_SFULL));
+        ptx::mma_commit(bar(Q_SFULL));
         return true;
       };
-      auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T
-        const uint64_t dv = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, j % STAGES) + TILE_BYTES, 16, 1024));
+      auto issue_dp = [&](int j) -> bool {  // dP(j) = dO V_j^T
+        const int sv = j % VSLOTS;
+        if (!wait(Q_VFULL + sv, (uint32_t)((j / VSLOTS) & 1))) return false;
+        ptx::tc_fence_after();
+        const uint64_t dv = ptx::launder(ptx::smem_desc_sw128(sbase + DQ_OFF_V + sv * TILE_BYTES, 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
           ptx::mma_ss(tdP, kmajor_step(dO0, kk), kmajor_step(dv, kk), ID_S, kk > 0 ? 1u : 0u);
-        ptx::mma_commit(bar(B_DPFULL));
+        ptx::mma_commit(bar(Q_DPFULL));
+        ptx::mma_commit(bar(Q_VEMPTY + sv));
+        return true;
       };
-      bool ok = wait(B_RES, 0);
+      bool ok = wait(Q_RES, 0);
       if (ok) ok = issue_s(0);
-      if (ok) issue_dp(0);
+      if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < T; ++j) {
         if (j + 1 < T) {
-          if (!(ok = wait(B_PREADY, (uint32_t)(j & 1)))) break;   // S(j) read by the warps
+          if (!(ok = wait(Q_SFREE, (uint32_t)(j & 1)))) break;    // S(j) read by the warps
           if (!(ok = issue_s(j + 1))) break;
-          if (!(ok = wait(B_DPFREE, (uint32_t)(j & 1)))) break;   // dP(j) read by the warps
-          issue_dp(j + 1);
+          if (!(ok = wait(Q_DPFREE, (uint32_t)(j & 1)))) break;   // dP(j) read by the warps
+          if (!(ok = issue_dp(j + 1))) break;
         }
-        if (!(ok = wait(B_DSREADY + (j & 1), (uint32_t)((j >> 1) & 1)))) break;
+        if (!(ok = wait(Q_DSREADY + (j & 1), (uint32_t)((j >> 1) & 1)))) break;
         ptx::tc_fence_after();
-        const uint64_t bk = ptx::launder(ptx::smem_desc_sw128(stage_addr(sbase, j % STAGES), HALF_BYTES, 1024));
+        const int sk = j % KSLOTS;
+        const uint64_t bk = ptx::launder(ptx::smem_desc_sw128(sbase + DQ_OFF_K + sk * TILE_BYTES, HALF_BYTES, 1024));
         const uint32_t ds = ptx::launder(tdS + 64 * (j & 1));
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)  // dQ += dS K (K = keys)
           ptx::mma_ts(tdQ, ds + kk * 8, bk + (uint64_t)((kk * 2048) >> 4), ID_G, (j > 0 || kk > 0) ? 1u : 0u);
-        ptx::mma_commit(bar(B_EMPTY + j % STAGES));
-        ptx::mma_commit(bar(B_DQDONE + (j & 1)));
+        ptx::mma_commit(bar(Q_KEMPTY + sk));
+        ptx::mma_commit(bar(Q_DQDONE + (j & 1)));
       }
-      if (ok) ptx::mma_commit(bar(B_ODONE));
-      ptx::mma_commit(bar(B_MMADONE));
-      ptx::mbar_drain(bar(B_MMADONE), 0, 200000000ull);
+      if (ok) ptx::mma_commit(bar(Q_ODONE));
+      ptx::mma_commit(bar(Q_MMADONE));
+      ptx::mbar_drain(bar(Q_MMADONE), 0, 200000000ull);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(REGS_ELEM) : "memory");
@@ -467,12 +542,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-      if (!(ok = wait(B_SFULL, (uint32_t)(j & 1)))) break;
+      if (!(ok = wait(Q_SFULL, (uint32_t)(j & 1)))) break;
       ptx::tc_fence_after();
       uint32_t r[64];
       ptx::tmem_ld64(tS + lane_bits + c0, r);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_PREADY));     // S(j) may now be overwritten
+      ptx::mbar_arrive(bar(Q_SFREE));      // S(j) may now be overwritten
       const int valid = tile_ref(p, j).valid - c0;  // key columns of this warpgroup that exist
       if (valid < 64) {
 #pragma unroll
@@ -488,11 +563,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         pv[2 * c] = ptx::ex2(x0);
         pv[2 * c + 1] = ptx::ex2(x1);
       }
-      if (!(ok = wait(B_DPFULL, (uint32_t)(j & 1)))) break;
+      if (!(ok = wait(Q_DPFULL, (uint32_t)(j & 1)))) break;
       ptx::tc_fence_after();
       ptx::tmem_ld64(tdP + lane_bits + c0, r);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_DPFREE));     // dP(j) may now be overwritten
+      ptx::mbar_arrive(bar(Q_DPFREE));     // dP(j) may now be overwritten
       uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
@@ -503,14 +578,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         pk[c] = ptx::bf16x2(d0, d1);
       }
       // dS(j) goes to buffer j % 2 once the dQ GEMM of tile j - 2 has read it
-      if (j >= 2 && !(ok = wait(B_DQDONE + (j & 1), (uint32_t)(((j - 2) >> 1) & 1)))) break;
+      if (j >= 2 && !(ok = wait(Q_DQDONE + (j & 1), (uint32_t)(((j - 2) >> 1) & 1)))) break;
       ptx::tc_fence_after();
       ptx::tmem_st32(tdS + lane_bits + 64 * (j & 1) + 32 * wg, pk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(B_DSREADY + (j & 1)));
+      ptx::mbar_arrive(bar(Q_DSREADY + (j & 1)));
     }
-    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
+    if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(Q_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
     if (ok) {
       ptx::tc_fence_after();
       store_row64(reinterpret_cast<__nv_bfloat16*>(p.dst0) + grow * HD + c0, tdQ + lane_bits + c0, p.scale,
@@ -598,7 +673,7 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(usp_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(usp_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(usp_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -632,7 +707,7 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   if (e != cudaSuccess) return e;
   p.dst0 = a.dq;
   p.dst1 = nullptr;
-  usp_bwd_dq_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
+  usp_bwd_dq_kernel<<<grid, NUM_THREADS, DQ_SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
   return cudaGetLastError();
 }
 
