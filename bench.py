@@ -305,6 +305,22 @@ class Step:
         return h2d, d2h
 
 
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    summary (profiles/traffic.json), or None when the kernel's source changed
+    since the counters were taken."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel, {}).get(workload)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "diffusion_transformer_sequence_gb300", "csrc", d["source"])
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["dram_bytes_per_launch"] if h == d["source_sha256_16"] else None
+
+
 def time_rows(w, reps=10):
     """Per-row GB/s of the bandwidth-bound entry points on this workload (L2 flushed)."""
     import diffusion_transformer_sequence_gb300 as usp
@@ -349,6 +365,12 @@ def our_arm(args, w, ws, rank, local):
     peaks = load_peaks()
     step = Step(w, backward=not args.no_backward)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    L = usp.lib()
+    import ctypes
+    phase_ms = (ctypes.c_float * 8)()
+    bwd_phases = []                      # per step: [prep, dK/dV kernel, dQ kernel] ms
+    if step.backward:
+        _lib_check(L.usp_profile_phases(1))
     with ClockSampler(local) as clocks:
         for _ in range(args.warmup):
             step.flush()
@@ -362,8 +384,13 @@ def our_arm(args, w, ws, rank, local):
         for i in range(args.steps):
             step.flush()
             step.run(evs[i], only=args.only)
+            if step.backward and args.only in (None, "backward"):
+                n = L.usp_profile_read(phase_ms, 8)   # waits for this step's last kernel
+                bwd_phases.append([phase_ms[k] * 1e-3 for k in range(n)])
         torch.cuda.synchronize()
         clocks.mark("end")
+    if step.backward:
+        _lib_check(L.usp_profile_phases(0))
     barrier(ws)
     if usp.device_status() != 0:
         raise RuntimeError("device error status during the timed steps")
@@ -399,9 +426,22 @@ def our_arm(args, w, ws, rank, local):
     mat_s = statistics.mean(mat)
     fused_tflops = w.fwd_flop / fused_s / 1e12
     peak = peaks["bf16_tflops"]
-    roofline = {"kernel": "attn_tc_fwd_kernel (fused USP forward, one launch)", "bound": "tensor",
-                "achieved": fused_tflops, "peak": peak, "unit": "TFLOP/s", "frac": fused_tflops / peak,
-                "traffic": None, "peak_kind": f"bf16 dense burst, {peaks['source']}"}
+    # the dominant kernel of the step: the one with the largest device time per step
+    kernels = {"attn_tc_fwd_kernel": (fused_s, w.fwd_flop, "fused USP forward (one launch per call)")}
+    if bwd_phases and len(bwd_phases[0]) == 3:
+        dkdv_s = statistics.mean(p[1] for p in bwd_phases)
+        dq_s = statistics.mean(p[2] for p in bwd_phases)
+        # algorithmic work: dK/dV kernel = 4 of the 5 backward GEMMs (S, dP, dV, dK);
+        # dQ kernel = the dQ GEMM (its recomputation of S and dP is not counted)
+        kernels["usp_bwd_dkdv_kernel"] = (dkdv_s, 0.8 * w.bwd_flop, "backward dK/dV (S^T, dP^T, dV, dK GEMMs)")
+        kernels["usp_bwd_dq_kernel"] = (dq_s, 0.2 * w.bwd_flop, "backward dQ (dQ GEMM; S, dP recompute uncounted)")
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    t_dom, f_dom, desc = kernels[dom]
+    ach = f_dom / t_dom / 1e12
+    roofline = {"kernel": f"{dom}: {desc}", "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": kernel_traffic(dom, w.name),
+                "launch_ms": t_dom * 1e3, "algorithmic_flop_per_launch": f_dom,
+                "peak_kind": f"bf16 dense burst, {peaks['source']} (sustained {peaks['bf16_tflops_sustained']})"}
     for k, r in rows.items():
         r["frac_of_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
     cpu = None
@@ -425,6 +465,8 @@ def our_arm(args, w, ws, rank, local):
                  "materialised_fwd_tflops": w.fwd_flop / mat_s / 1e12, "fused_fwd_tflops": fused_tflops,
                  **({"bwd_ms": statistics.mean(bwd) * 1e3,
                      "bwd_tflops": w.bwd_flop / statistics.mean(bwd) / 1e12} if step.backward else {}),
+                 **({k + "_ms": v[0] * 1e3 for k, v in kernels.items()}),
+                 **({k + "_tflops": v[1] / v[0] / 1e12 for k, v in kernels.items()}),
                  **{k + "_GBps": v["GB/s"] for k, v in rows.items()},
                  **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items()}},
         "roofline": roofline,
@@ -435,6 +477,11 @@ def our_arm(args, w, ws, rank, local):
         "peaks": peaks,
     }
     print(json.dumps(line), flush=True)
+
+
+def _lib_check(rc):
+    from diffusion_transformer_sequence_gb300 import _lib
+    _lib.check("usp_profile", rc)
 
 
 def main():

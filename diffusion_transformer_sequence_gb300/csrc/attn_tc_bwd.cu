@@ -683,6 +683,7 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
       (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, a.delta, a.l2, rows, a.Ns, Ns_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  phase_mark(stream);
   CUtensorMap mq, mk, mv, mdo, ml2, mdl;
   if (!map_stack_bf16(&mq, a.q, a.Ns, a.BH, a.sp) || !map_stack_bf16(&mk, a.k, a.Ns, a.BH, a.sp) ||
       !map_stack_bf16(&mv, a.v, a.Ns, a.BH, a.sp) || !map_stack_bf16(&mdo, a.dout, a.Ns, a.BH, a.sp) ||
@@ -705,10 +706,13 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   usp_bwd_dkdv_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mdo, ml2, mdl, p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  phase_mark(stream);
   p.dst0 = a.dq;
   p.dst1 = nullptr;
   usp_bwd_dq_kernel<<<grid, NUM_THREADS, DQ_SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  phase_mark(stream);
+  return e;
 }
 
 }  // namespace usp

@@ -24,6 +24,29 @@ __device__ unsigned int g_dev_error = 0;
 namespace {
 
 thread_local int t_last_cuda_error = 0;
+
+// Phase timing (usp_profile_phases / usp_profile_read): events recorded at the
+// kernel boundaries of the most recent attention call on this thread.
+constexpr int kMaxPhases = 8;
+struct PhaseState {
+  bool enabled = false;
+  bool created = false;
+  int marks = 0;
+  cudaEvent_t ev[kMaxPhases + 1];
+};
+thread_local PhaseState t_phase;
+
+}  // namespace
+void phase_mark(cudaStream_t s) {
+  if (!t_phase.enabled || t_phase.marks == 0 || t_phase.marks > kMaxPhases) return;
+  if (cudaEventRecord(t_phase.ev[t_phase.marks], s) == cudaSuccess) ++t_phase.marks;
+}
+namespace {
+void phase_begin(cudaStream_t s) {
+  if (!t_phase.enabled) return;
+  t_phase.marks = 0;
+  if (cudaEventRecord(t_phase.ev[0], s) == cudaSuccess) t_phase.marks = 1;
+}
 std::atomic<long long> g_spin_limit{-1};
 constexpr long long kDefaultSpinLimit = 1LL << 40;       // polls; the time bound below governs
 constexpr unsigned long long kWaitNs = 2000000000ull;    // 2 s per wait
@@ -258,7 +281,9 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
       a.fused = true;
       a.BH = B * H; a.sp = sp; a.Ns = Ns;
       a.scale = scale;
+      phase_begin(s);
       e = launch_attn_tc_fwd(a, g, s);
+      phase_mark(s);
     }
     return e == cudaSuccess ? USP_OK : cuda_fail(e);
   }
@@ -270,21 +295,27 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
   if (!aligned(workspace, 256)) return USP_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
   const int elt = (int)elt_size(dtype);
+  phase_begin(s);
   if ((st = relayout(q, ws + w.xq, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
   if ((st = relayout(k, ws + w.xk, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
   if ((st = relayout(v, ws + w.xv, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
+  phase_mark(s);
   void* o_dst = r > 1 ? (void*)(ws + w.parts_o) : (void*)(ws + w.xo);
   float* l_dst = r > 1 ? (float*)(ws + w.parts_l) : (float*)(ws + w.xl);
   if ((st = chunk_attention(ws + w.xq, ws + w.xk, ws + w.xv, o_dst, l_dst, B, Hu, Nr, D, u, r, scale, dtype, s)) !=
       USP_OK)
     return st;
+  phase_mark(s);
   if (r > 1) {
     cudaError_t e = launch_lse_merge(ws + w.parts_o, (const float*)(ws + w.parts_l), r, ws + w.xo,
                                      (float*)(ws + w.xl), B * H * N, D, (int)dtype, s);
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  phase_mark(s);
   if ((st = relayout(ws + w.xo, out, B, H, N, D, u, r, elt, false, s)) != USP_OK) return st;
-  return relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s);
+  st = relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s);
+  phase_mark(s);
+  return st;
 }
 
 int usp_attention_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
@@ -325,7 +356,8 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
     a.delta = delta; a.l2 = l2;
     a.BH = B * H; a.sp = sp; a.Ns = Ns;
     a.scale = scale;
-    e = launch_attn_tc_bwd(a, g, s);
+    phase_begin(s);
+    e = launch_attn_tc_bwd(a, g, s);  // marks a phase after each of its three kernels
   }
   return e == cudaSuccess ? USP_OK : cuda_fail(e);
 }
@@ -364,5 +396,30 @@ const char* usp_status_string(int status) {
 int usp_last_cuda_error(void) { return t_last_cuda_error; }
 
 void usp_set_spin_limit(long long polls) { g_spin_limit.store(polls < 0 ? -1 : polls); }
+
+int usp_profile_phases(int enable) {
+  if (enable && !t_phase.created) {
+    for (int i = 0; i <= kMaxPhases; ++i) {
+      cudaError_t e = cudaEventCreate(&t_phase.ev[i]);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    t_phase.created = true;
+  }
+  t_phase.enabled = enable != 0;
+  t_phase.marks = 0;
+  return USP_OK;
+}
+
+int usp_profile_read(float* ms, int max_phases) {
+  if (!t_phase.created || t_phase.marks < 2) return 0;
+  const int n = t_phase.marks - 1;
+  cudaError_t e = cudaEventSynchronize(t_phase.ev[n]);
+  if (e != cudaSuccess) return -cuda_fail(e);
+  for (int i = 0; i < n && i < max_phases; ++i) {
+    e = cudaEventElapsedTime(&ms[i], t_phase.ev[i], t_phase.ev[i + 1]);
+    if (e != cudaSuccess) return -cuda_fail(e);
+  }
+  return n < max_phases ? n : max_phases;
+}
 
 }  // extern "C"

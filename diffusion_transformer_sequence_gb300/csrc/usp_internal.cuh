@@ -86,6 +86,8 @@ cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, 
                                 float* delta, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
                                 cudaStream_t stream);
 
-Guard current_guard();  // the guard for the current device (error word + limits)
+// Records the next phase event of the current call (no-op unless phase timing
+// is enabled with usp_profile_phases).
+void phase_mark(cudaStream_t s);
 
 }  // namespace usp

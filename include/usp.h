@@ -176,6 +176,21 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
                               int64_t H, int64_t N, int64_t D, int ulysses, int ring, float scale,
                               usp_dtype dtype, usp_stream_t stream);
 
+/* Phase timing for profiling: while enabled (enable = 1), each later
+ * usp_attention_fwd / usp_attention_bwd call on this thread records a CUDA
+ * event on its stream before its first kernel and after each kernel group:
+ *   fused forward:        [attention]
+ *   materialised forward: [tok2head x3] [chunk attention] [merge] [head2tok x2]
+ *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
+ * (the fp32 paths record nothing).  The events
+ * are created by the library on first enable.  Returns USP_OK or USP_ERR_CUDA. */
+int usp_profile_phases(int enable);
+
+/* Waits for the last event of the most recent recorded call on this thread
+ * and writes the milliseconds of each of its phases to ms[0 .. n-1]; returns
+ * n (<= max_phases), 0 if nothing was recorded, or -USP_ERR_CUDA. */
+int usp_profile_read(float* ms, int max_phases);
+
 /* Synchronises `stream`, then reads and clears the current device's error
  * word.  Returns USP_OK, USP_ERR_TIMEOUT if a bounded device wait expired
  * since the last call, or USP_ERR_CUDA. */
