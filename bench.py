@@ -233,7 +233,9 @@ class Step:
             usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
                               mode="fused", out=self.out_f, lse=self.lse_f)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-        self.launches_per_step = (7 if w.ring > 1 else 6) + 1 + (3 if backward else 0)
+        # materialised: tok2head (q, k, v in one launch), chunk attention, merge (ring > 1), head2tok x2;
+        # fused: one; backward: prep + dK/dV + dQ
+        self.launches_per_step = (5 if w.ring > 1 else 4) + 1 + (3 if backward else 0)
 
     def flop(self):
         f = 2 * self.w.fwd_flop

@@ -48,18 +48,20 @@ __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float
 __device__ __forceinline__ void from_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void from_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-// Row statistics shared by both kernels: returns L, fills w[t] = exp(lse_t - L).
+// Row statistics: returns L, fills w[t] = exp(lse_t - L).  Computed with the
+// hardware exp2 / log2 approximations (relative error ~1e-7, far inside the
+// merge's fp32 and bf16 tolerances) to keep the kernel memory-bound.
 template <int kMaxR>
 __device__ __forceinline__ float merge_weights(const float* __restrict__ lses, int R, int64_t rows,
                                                int64_t row, float* w) {
   float m = -INFINITY;
   for (int t = 0; t < R; ++t) m = fmaxf(m, __ldg(lses + t * rows + row));
   float s = 0.f;
-  for (int t = 0; t < R; ++t) s += expf(__ldg(lses + t * rows + row) - m);
-  const float L = m + logf(s);
+  for (int t = 0; t < R; ++t) s += __expf(__ldg(lses + t * rows + row) - m);
+  const float L = m + __logf(s);
 #pragma unroll
   for (int t = 0; t < kMaxR; ++t)
-    if (t < R) w[t] = expf(__ldg(lses + t * rows + row) - L);
+    if (t < R) w[t] = __expf(__ldg(lses + t * rows + row) - L);
   return L;
 }
 

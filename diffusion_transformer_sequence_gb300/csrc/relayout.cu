@@ -22,11 +22,18 @@ constexpr int kUnroll = 4;
 template <typename Vec>
 __device__ __forceinline__ Vec load_stream(const Vec* p) { return __ldg(p); }
 
+// Up to three tensors of the same shape per launch (blockIdx.z picks one):
+// q, k and v of the materialised forward go through one launch.
+struct Tensors {
+  const void* src[3];
+  void* dst[3];
+};
+
 template <typename Vec, bool kTok2Head>
-__global__ void __launch_bounds__(kThreads) relayout_kernel(const Vec* __restrict__ src,
-                                                            Vec* __restrict__ dst, int64_t nruns,
-                                                            int64_t run_vecs, int64_t B, int64_t H,
-                                                            int64_t Hu, int64_t u) {
+__global__ void __launch_bounds__(kThreads) relayout_kernel(Tensors ts, int64_t nruns, int64_t run_vecs,
+                                                            int64_t B, int64_t H, int64_t Hu, int64_t u) {
+  const Vec* __restrict__ src = static_cast<const Vec*>(ts.src[blockIdx.z]);
+  Vec* __restrict__ dst = static_cast<Vec*>(ts.dst[blockIdx.z]);
   for (int64_t run = blockIdx.y; run < nruns; run += gridDim.y) {
     int64_t src_run;
     if (kTok2Head) {
@@ -68,38 +75,49 @@ __global__ void __launch_bounds__(kThreads) relayout_kernel(const Vec* __restric
 }
 
 template <typename Vec>
-cudaError_t launch_vec(const void* src, void* dst, int64_t nruns, int64_t run_bytes, int64_t B,
-                       int64_t H, int64_t Hu, int64_t u, bool tok2head, cudaStream_t stream) {
+cudaError_t launch_vec(const Tensors& ts, int count, int64_t nruns, int64_t run_bytes, int64_t B, int64_t H,
+                       int64_t Hu, int64_t u, bool tok2head, cudaStream_t stream) {
   const int64_t run_vecs = run_bytes / (int64_t)sizeof(Vec);
   const int64_t per_cta = (int64_t)kThreads * kUnroll;
   int64_t gx = (run_vecs + per_cta - 1) / per_cta;
   if (gx > 1024) gx = 1024;
   int64_t gy = nruns < 65535 ? nruns : 65535;
-  dim3 grid((unsigned)gx, (unsigned)gy, 1);
+  dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)count);
   if (tok2head)
-    relayout_kernel<Vec, true><<<grid, kThreads, 0, stream>>>((const Vec*)src, (Vec*)dst, nruns,
-                                                             run_vecs, B, H, Hu, u);
+    relayout_kernel<Vec, true><<<grid, kThreads, 0, stream>>>(ts, nruns, run_vecs, B, H, Hu, u);
   else
-    relayout_kernel<Vec, false><<<grid, kThreads, 0, stream>>>((const Vec*)src, (Vec*)dst, nruns,
-                                                              run_vecs, B, H, Hu, u);
+    relayout_kernel<Vec, false><<<grid, kThreads, 0, stream>>>(ts, nruns, run_vecs, B, H, Hu, u);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_relayout(const void* src, void* dst, int64_t /*runs_outer*/, int64_t B, int64_t H,
-                            int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
-                            cudaStream_t stream) {
+cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
+                              int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
+                              cudaStream_t stream) {
+  if (count < 1 || count > 3) return cudaErrorInvalidValue;
   const int64_t u = ulysses;
   const int64_t Hu = H / u;
   const int64_t nruns = (int64_t)ring * u * B * H;
   const int64_t run_bytes = Ns * D * elt;
-  const uintptr_t a = (uintptr_t)src | (uintptr_t)dst | (uintptr_t)run_bytes;
-  if ((a & 15) == 0) return launch_vec<uint4>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
-  if ((a & 7) == 0) return launch_vec<uint2>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
-  if ((a & 3) == 0) return launch_vec<uint32_t>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
-  if ((a & 1) == 0) return launch_vec<uint16_t>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
-  return launch_vec<uint8_t>(src, dst, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  Tensors ts{};
+  uintptr_t a = (uintptr_t)run_bytes;
+  for (int i = 0; i < count; ++i) {
+    ts.src[i] = srcs[i];
+    ts.dst[i] = dsts[i];
+    a |= (uintptr_t)srcs[i] | (uintptr_t)dsts[i];
+  }
+  if ((a & 15) == 0) return launch_vec<uint4>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  if ((a & 7) == 0) return launch_vec<uint2>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  if ((a & 3) == 0) return launch_vec<uint32_t>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  if ((a & 1) == 0) return launch_vec<uint16_t>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+  return launch_vec<uint8_t>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+}
+
+cudaError_t launch_relayout(const void* src, void* dst, int64_t /*runs_outer*/, int64_t B, int64_t H,
+                            int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
+                            cudaStream_t stream) {
+  return launch_relayout_n(&src, &dst, 1, B, H, Ns, D, ulysses, ring, elt, tok2head, stream);
 }
 
 }  // namespace usp

@@ -296,9 +296,12 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
   char* ws = static_cast<char*>(workspace);
   const int elt = (int)elt_size(dtype);
   phase_begin(s);
-  if ((st = relayout(q, ws + w.xq, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
-  if ((st = relayout(k, ws + w.xk, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
-  if ((st = relayout(v, ws + w.xv, B, H, N, D, u, r, elt, true, s)) != USP_OK) return st;
+  {  // q, k, v in one launch
+    const void* srcs[3] = {q, k, v};
+    void* dsts[3] = {ws + w.xq, ws + w.xk, ws + w.xv};
+    cudaError_t e = launch_relayout_n(srcs, dsts, 3, B, H, Ns, D, u, r, elt, true, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   phase_mark(s);
   void* o_dst = r > 1 ? (void*)(ws + w.parts_o) : (void*)(ws + w.xo);
   float* l_dst = r > 1 ? (float*)(ws + w.parts_l) : (float*)(ws + w.xl);

@@ -39,6 +39,11 @@ cudaError_t launch_relayout(const void* src, void* dst, int64_t runs_outer, int6
                             int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                             cudaStream_t stream);
 
+// The same re-layout of up to three same-shape tensors in one launch.
+cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
+                              int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
+                              cudaStream_t stream);
+
 cudaError_t launch_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
                              int64_t rows, int64_t D, int dtype, cudaStream_t stream);
 

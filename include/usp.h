@@ -180,7 +180,7 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  * usp_attention_fwd / usp_attention_bwd call on this thread records a CUDA
  * event on its stream before its first kernel and after each kernel group:
  *   fused forward:        [attention]
- *   materialised forward: [tok2head x3] [chunk attention] [merge] [head2tok x2]
+ *   materialised forward: [tok2head q,k,v] [chunk attention] [merge] [head2tok x2]
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
  * (the fp32 paths record nothing).  The events
  * are created by the library on first enable.  Returns USP_OK or USP_ERR_CUDA. */
