@@ -16,4 +16,5 @@ from .usp_oracle import (  # noqa: F401
     ring_chunk,
     tok2head,
     usp_forward,
+    usp_forward_joint,
 )

@@ -20,7 +20,12 @@ Sources (page titles as extracted):
   ring, Ulysses ranks contiguous, ring ranks strided), "Ring kernel
   selection" (kernels return LSE and pair with a real backward), Numerics.
 * [VO]  vllm-omni "Parallelism Acceleration Guide", "How to parallelize a new
-  model": tokens are chunked along the sequence by SP rank in rank order.
+  model": tokens are chunked along the sequence by SP rank in rank order;
+  Qwen-Image runs joint attention over concatenated text + image tokens and
+  keeps the text replicated on every SP rank while the image tokens are
+  chunked.  The handbook's token counts (FLUX 4608, Wan 76112) include 512
+  text tokens; the PR page notes that replicated text K/V make local
+  attention exact.
 
 Readings where the pages are silent or open:
 
@@ -38,6 +43,10 @@ Readings where the pages are silent or open:
   of its ring group in rank order along tokens.
 * No mask, no causal masking, no dropout; an explicit ``scale`` (1/sqrt(D)
   in every workload, SDPA's default).
+* Joint attention: the text K/V are one extra KV chunk, unsharded and the
+  same on every rank, merged with the ring chunks by the same log-sum-exp
+  merge; text queries (replicated) attend to the text chunk and to every
+  ring chunk of their Ulysses head group.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 library routines (torch fp64 SDPA and autograd on CPU), closed forms,
@@ -249,3 +258,55 @@ def attention_bwd_sampled(q, k, v, dout, scale: float, qrows, krows, row_block: 
         dv += Pc.T @ dout[r0:r1]
         dk += scale * (dSc.T @ q[r0:r1])
     return dq, dk, dv
+
+
+# ---------------------------------------------------------------------------
+# Joint attention with replicated text tokens ([VO] Qwen-Image; [PR] text K/V
+# replicated, local attention exact)
+# ---------------------------------------------------------------------------
+
+def usp_forward_joint(Tq, Tk, Tv, k_txt, v_txt, ulysses: int, ring: int, scale: float, q_txt=None):
+    """Joint USP attention: image tokens sharded, text tokens replicated.
+
+    Tq/Tk/Tv: token-sharded image stacks [ring, ulysses, B, H, Ns, D];
+    k_txt/v_txt (and q_txt): text tensors [B, H, Nt, D], the same on every
+    rank.  Per virtual rank (g, j), after the Ulysses re-layout, the image
+    queries attend to every ring chunk c = (g - t) mod ring of their head
+    group (t = 0..ring-1) and to the text chunk of their head group; the
+    ring + 1 partials are merged by log-sum-exp and re-laid out.  Text
+    queries of head group j attend to the text chunk and to the ring chunks
+    of head group j (identical on every ring rank, computed once).
+    Returns (O, LSE) in the image stack layout and, when q_txt is given,
+    (O_txt [B, H, Nt, D], LSE_txt [B, H, Nt]).
+    """
+    Xq = tok2head(np.asarray(Tq, dtype=np.float64), ulysses, ring)
+    Xk = tok2head(np.asarray(Tk, dtype=np.float64), ulysses, ring)
+    Xv = tok2head(np.asarray(Tv, dtype=np.float64), ulysses, ring)
+    kt = np.asarray(k_txt, dtype=np.float64)
+    vt = np.asarray(v_txt, dtype=np.float64)
+    Hu = Xq.shape[3]
+    parts_o = np.empty((ring + 1,) + Xq.shape, dtype=np.float64)
+    parts_l = np.empty((ring + 1,) + Xq.shape[:-1], dtype=np.float64)
+    for g in range(ring):
+        for j in range(ulysses):
+            hs = slice(j * Hu, (j + 1) * Hu)
+            for t in range(ring):
+                c = ring_chunk(g, t, ring)
+                parts_o[t, g, j], parts_l[t, g, j] = attention(Xq[g, j], Xk[c, j], Xv[c, j], scale)
+            parts_o[ring, g, j], parts_l[ring, g, j] = attention(Xq[g, j], kt[:, hs], vt[:, hs], scale)
+    Xo, Xl = lse_merge(parts_o, parts_l)
+    out = (head2tok(Xo, ulysses, ring), head2tok(Xl, ulysses, ring))
+    if q_txt is None:
+        return out
+    qt = np.asarray(q_txt, dtype=np.float64)
+    o_txt = np.empty(qt.shape, dtype=np.float64)
+    l_txt = np.empty(qt.shape[:-1], dtype=np.float64)
+    for j in range(ulysses):
+        hs = slice(j * Hu, (j + 1) * Hu)
+        po = np.empty((ring + 1,) + qt[:, hs].shape, dtype=np.float64)
+        pl = np.empty((ring + 1,) + qt[:, hs].shape[:-1], dtype=np.float64)
+        for c in range(ring):
+            po[c], pl[c] = attention(qt[:, hs], Xk[c, j], Xv[c, j], scale)
+        po[ring], pl[ring] = attention(qt[:, hs], kt[:, hs], vt[:, hs], scale)
+        o_txt[:, hs], l_txt[:, hs] = lse_merge(po, pl)
+    return out + (o_txt, l_txt)

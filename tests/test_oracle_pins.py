@@ -192,6 +192,23 @@ def test_usp_forward_equals_unsharded(u, r, H, N):
     np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(L)).numpy(), rl.numpy(), atol=1e-12)
 
 
+@pytest.mark.parametrize("u,r,H,N,Nt", [(2, 2, 4, 24, 5), (1, 3, 2, 18, 7), (4, 1, 8, 16, 3), (1, 1, 2, 8, 1)])
+def test_usp_joint_equals_attention_over_concatenated_tokens(u, r, H, N, Nt):
+    """Joint attention with replicated text == unsharded attention over [text; image]."""
+    B, D, scale = 2, 8, 0.3
+    q, k, v = _rand((B, H, N, D), 150), _rand((B, H, N, D), 151), _rand((B, H, N, D), 152)
+    qt, kt, vt = _rand((B, H, Nt, D), 153), _rand((B, H, Nt, D), 154), _rand((B, H, Nt, D), 155)
+    T = [wl.to_token_stack(x, u, r).numpy() for x in (q, k, v)]
+    O, L, Ot, Lt = uo.usp_forward_joint(*T, kt.numpy(), vt.numpy(), u, r, scale, q_txt=qt.numpy())
+    K, V = torch.cat([kt, k], 2), torch.cat([vt, v], 2)
+    ro, rl = _sdpa(q, K, V, scale)
+    np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(O)).numpy(), ro.numpy(), atol=1e-12)
+    np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(L)).numpy(), rl.numpy(), atol=1e-12)
+    to, tl = _sdpa(qt, K, V, scale)
+    np.testing.assert_allclose(Ot, to.numpy(), atol=1e-12)
+    np.testing.assert_allclose(Lt, tl.numpy(), atol=1e-12)
+
+
 def test_ring_chunk_schedule_visits_every_chunk_once():
     for r in range(1, 9):
         for g in range(r):
@@ -289,6 +306,12 @@ def _pins_pass(mod) -> bool:
         O, L = mod.usp_forward(*T, 2, 2, 0.5)
         if not np.allclose(wl.from_token_stack(torch.from_numpy(O)).numpy(), ro.numpy(), atol=1e-10):
             return False
+        kt, vt = rng.standard_normal((2, 2, 3, 4)), rng.standard_normal((2, 2, 3, 4))
+        Oj, Lj = mod.usp_forward_joint(*T, kt, vt, 2, 2, 0.5)
+        rj, _ = _sdpa(torch.from_numpy(q), torch.from_numpy(np.concatenate([kt, k], 2)),
+                      torch.from_numpy(np.concatenate([vt, v], 2)), 0.5)
+        if not np.allclose(wl.from_token_stack(torch.from_numpy(Oj)).numpy(), rj.numpy(), atol=1e-10):
+            return False
         oo, ll = uo.attention(q, k, v, 0.5)
         do = rng.standard_normal(q.shape)
         qt, kt, vt = (torch.from_numpy(a).requires_grad_() for a in (q, k, v))
@@ -319,6 +342,7 @@ MUTATIONS = [
     ("= T[g, s, :, j * Hu:(j + 1) * Hu]", "= T[g, j, :, s * Hu:(s + 1) * Hu]"),                   # swapped rank roles
     ("X[g, j, :, :, s * Ns:(s + 1) * Ns] = T", "X[g, (j + 1) % u, :, :, s * Ns:(s + 1) * Ns] = T"),  # wrong destination
     ("return (g - t) % ring", "return g"),                                                         # no ring rotation
+    ("    Xo, Xl = lse_merge(parts_o, parts_l)\n    out =", "    Xo, Xl = lse_merge(parts_o[:ring], parts_l[:ring])\n    out ="),  # text chunk dropped
     ("dS = P * (dP - delta[..., None])", "dS = P * (dP + delta[..., None])"),                    # wrong sign
     ("dk = scale * (np.swapaxes(dS, -1, -2) @ q)", "dk = scale * (np.swapaxes(dS, -1, -2) @ k)"), # wrong operand
     ("dv = np.swapaxes(P, -1, -2) @ dout", "dv = P @ dout"),                                      # missing transpose
