@@ -15,6 +15,7 @@ from .usp_oracle import (  # noqa: F401
     lse_merge,
     ring_chunk,
     tok2head,
+    usp_cross_attention,
     usp_forward,
     usp_forward_joint,
 )

@@ -47,6 +47,8 @@ Readings where the pages are silent or open:
   same on every rank, merged with the ring chunks by the same log-sum-exp
   merge; text queries (replicated) attend to the text chunk and to every
   ring chunk of their Ulysses head group.
+* Cross-attention: each rank's image queries attend to the replicated text
+  K/V only; nothing is exchanged.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 library routines (torch fp64 SDPA and autograd on CPU), closed forms,
@@ -310,3 +312,25 @@ def usp_forward_joint(Tq, Tk, Tv, k_txt, v_txt, ulysses: int, ring: int, scale: 
         po[ring], pl[ring] = attention(qt[:, hs], kt[:, hs], vt[:, hs], scale)
         o_txt[:, hs], l_txt[:, hs] = lse_merge(po, pl)
     return out + (o_txt, l_txt)
+
+
+def usp_cross_attention(Tq, k_txt, v_txt, ulysses: int, ring: int, scale: float):
+    """Cross-attention under sequence parallelism: image queries sharded,
+    text K/V replicated.
+
+    Tq: token-sharded query stack [ring, ulysses, B, H, Ns, D]; k_txt, v_txt:
+    [B, H, Nt, D], the same on every rank.  Every virtual rank attends its own
+    query tokens to the complete text K/V, so no exchange is needed and the
+    local result is already exact (the PR page: replicated K/V make local
+    attention exact).  Returns (O, LSE) in the stack layout.
+    """
+    Tq = np.asarray(Tq, dtype=np.float64)
+    kt = np.asarray(k_txt, dtype=np.float64)
+    vt = np.asarray(v_txt, dtype=np.float64)
+    O = np.empty(Tq.shape, dtype=np.float64)
+    L = np.empty(Tq.shape[:-1], dtype=np.float64)
+    for g in range(ring):
+        for j in range(ulysses):
+            O[g, j], L[g, j] = attention(Tq[g, j], kt, vt, scale)
+    return O, L
+

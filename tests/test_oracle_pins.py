@@ -209,6 +209,19 @@ def test_usp_joint_equals_attention_over_concatenated_tokens(u, r, H, N, Nt):
     np.testing.assert_allclose(Lt, tl.numpy(), atol=1e-12)
 
 
+@pytest.mark.parametrize("u,r,N,Nt", [(2, 2, 16, 5), (4, 1, 12, 7), (1, 3, 9, 1)])
+def test_usp_cross_attention_equals_unsharded(u, r, N, Nt):
+    """Cross-attention of sharded image queries to replicated text K/V ==
+    unsharded SDPA of all image queries against the text."""
+    B, H, D, scale = 2, 4, 8, 0.4
+    q = _rand((B, H, N, D), 160)
+    kt, vt = _rand((B, H, Nt, D), 161), _rand((B, H, Nt, D), 162)
+    O, L = uo.usp_cross_attention(wl.to_token_stack(q, u, r).numpy(), kt.numpy(), vt.numpy(), u, r, scale)
+    ro, rl = _sdpa(q, kt, vt, scale)
+    np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(O)).numpy(), ro.numpy(), atol=1e-12)
+    np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(L)).numpy(), rl.numpy(), atol=1e-12)
+
+
 def test_ring_chunk_schedule_visits_every_chunk_once():
     for r in range(1, 9):
         for g in range(r):
@@ -307,10 +320,18 @@ def _pins_pass(mod) -> bool:
         if not np.allclose(wl.from_token_stack(torch.from_numpy(O)).numpy(), ro.numpy(), atol=1e-10):
             return False
         kt, vt = rng.standard_normal((2, 2, 3, 4)), rng.standard_normal((2, 2, 3, 4))
-        Oj, Lj = mod.usp_forward_joint(*T, kt, vt, 2, 2, 0.5)
-        rj, _ = _sdpa(torch.from_numpy(q), torch.from_numpy(np.concatenate([kt, k], 2)),
-                      torch.from_numpy(np.concatenate([vt, v], 2)), 0.5)
+        qtx = rng.standard_normal((2, 2, 3, 4))
+        Oj, Lj, Otj, Ltj = mod.usp_forward_joint(*T, kt, vt, 2, 2, 0.5, q_txt=qtx)
+        Kc, Vc = torch.from_numpy(np.concatenate([kt, k], 2)), torch.from_numpy(np.concatenate([vt, v], 2))
+        rj, _ = _sdpa(torch.from_numpy(q), Kc, Vc, 0.5)
         if not np.allclose(wl.from_token_stack(torch.from_numpy(Oj)).numpy(), rj.numpy(), atol=1e-10):
+            return False
+        rtj, _ = _sdpa(torch.from_numpy(qtx), Kc, Vc, 0.5)
+        if not np.allclose(Otj, rtj.numpy(), atol=1e-10):
+            return False
+        Oc, _ = mod.usp_cross_attention(T[0], kt, vt, 2, 2, 0.5)
+        rc, _ = _sdpa(torch.from_numpy(q), torch.from_numpy(kt), torch.from_numpy(vt), 0.5)
+        if not np.allclose(wl.from_token_stack(torch.from_numpy(Oc)).numpy(), rc.numpy(), atol=1e-10):
             return False
         oo, ll = uo.attention(q, k, v, 0.5)
         do = rng.standard_normal(q.shape)
@@ -343,6 +364,8 @@ MUTATIONS = [
     ("X[g, j, :, :, s * Ns:(s + 1) * Ns] = T", "X[g, (j + 1) % u, :, :, s * Ns:(s + 1) * Ns] = T"),  # wrong destination
     ("return (g - t) % ring", "return g"),                                                         # no ring rotation
     ("    Xo, Xl = lse_merge(parts_o, parts_l)\n    out =", "    Xo, Xl = lse_merge(parts_o[:ring], parts_l[:ring])\n    out ="),  # text chunk dropped
+    ("po[c], pl[c] = attention(qt[:, hs], Xk[c, j]", "po[c], pl[c] = attention(qt[:, hs], Xk[c, (j + 1) % ulysses]"),  # text queries, wrong head group
+    ("O[g, j], L[g, j] = attention(Tq[g, j], kt", "O[g, j], L[g, j] = attention(Tq[g, (j + 1) % ulysses], kt"),  # cross: wrong rank's tokens
     ("dS = P * (dP - delta[..., None])", "dS = P * (dP + delta[..., None])"),                    # wrong sign
     ("dk = scale * (np.swapaxes(dS, -1, -2) @ q)", "dk = scale * (np.swapaxes(dS, -1, -2) @ k)"), # wrong operand
     ("dv = np.swapaxes(P, -1, -2) @ dout", "dv = P @ dout"),                                      # missing transpose
