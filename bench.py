@@ -133,17 +133,24 @@ def barrier(ws):
 
 # ---------------------------------------------------------------- reference arm
 def oracle_sample_flop(w, heads):
-    return 4.0 * w.B * heads * w.N * w.N * w.D
+    n = w.N + w.Nt
+    return 4.0 * w.B * heads * n * n * w.D
 
 
 def run_oracle_sample(w, heads: int):
-    """Time the CPU oracle's USP forward on `heads` heads of the workload."""
+    """Time the CPU oracle's USP forward (joint when the workload has text
+    tokens) on `heads` heads of the workload."""
     import oracle
-    sub = wl.custom(w.name, w.dtype, w.B, heads, w.N, w.D, w.ulysses, w.ring, seed=w.seed)
+    sub = wl.custom(w.name, w.dtype, w.B, heads, w.N, w.D, w.ulysses, w.ring, seed=w.seed, Nt=w.Nt)
     inp = wl.make_inputs(sub, with_dout=False)
     stacks = [wl.to_token_stack(inp[n], w.ulysses, w.ring).double().numpy() for n in ("q", "k", "v")]
     t0 = time.perf_counter()
-    oracle.usp_forward(*stacks, w.ulysses, w.ring, w.scale)
+    if w.Nt:
+        txt = {n: t.double().numpy() for n, t in wl.make_text_inputs(sub).items()}
+        oracle.usp_forward_joint(*stacks, txt["k_txt"], txt["v_txt"], w.ulysses, w.ring, w.scale,
+                                 q_txt=txt["q_txt"])
+    else:
+        oracle.usp_forward(*stacks, w.ulysses, w.ring, w.scale)
     return time.perf_counter() - t0
 
 
@@ -157,7 +164,7 @@ def cpu_cores():
 def sample_heads(w):
     """Heads of the workload the CPU-baseline leg runs (a multiple of ulysses):
     the whole workload when it is small, else about a quarter of its heads."""
-    if w.fwd_flop <= 0.25e12:
+    if oracle_sample_flop(w, w.H) <= 0.25e12:
         return w.H
     return min(w.H, max(w.ulysses, (w.H // 4) // w.ulysses * w.ulysses))
 
@@ -173,9 +180,14 @@ def reference_arm(args, w, ws, rank):
         return
     import numpy as np
     import oracle
-    sub = wl.custom(w.name, w.dtype, w.B, w.ulysses, w.N, w.D, w.ulysses, w.ring, seed=w.seed)
+    sub = wl.custom(w.name, w.dtype, w.B, w.ulysses, w.N, w.D, w.ulysses, w.ring, seed=w.seed, Nt=w.Nt)
     inp = wl.make_inputs(sub, with_dout=False)
     q, k, v = (inp[n][0, 0].double().numpy() for n in ("q", "k", "v"))
+    if w.Nt:   # joint: the image queries against the text + image keys of the head
+        txt = wl.make_text_inputs(sub)
+        k = np.concatenate([txt["k_txt"][0, 0].double().numpy(), k])
+        v = np.concatenate([txt["v_txt"][0, 0].double().numpy(), v])
+    nk = k.shape[0]
     ncal = min(256, w.N)
     t0 = time.perf_counter()
     oracle.attention_rows(q, k, v, np.arange(ncal), w.scale)
@@ -191,16 +203,17 @@ def reference_arm(args, w, ws, rank):
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
-    flop = 4.0 * rows * w.N * w.D
+    flop = 4.0 * rows * nk * w.D
     tflops = flop / statistics.mean(times) / 1e12
-    sample = (f"oracle attention (numpy fp64) of {rows} seeded query rows of one head against all N={w.N} keys "
+    sample = (f"oracle attention (numpy fp64) of {rows} seeded query rows of one head against all {nk} keys "
               f"of {w.name}, per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "desc": w.description, "global_batch": w.B, "seq_len": w.N,
-                   "ulysses": w.ulysses, "ring": w.ring, "parallelism": "virtual ranks on one device"},
+                   "text_len": w.Nt, "ulysses": w.ulysses, "ring": w.ring,
+                   "parallelism": "virtual ranks on one device"},
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -236,12 +249,49 @@ class Step:
         # materialised: tok2head (q, k, v in one launch), chunk attention, merge (ring > 1), head2tok x2;
         # fused: one; backward: prep + dK/dV + dQ
         self.launches_per_step = (5 if w.ring > 1 else 4) + 1 + (3 if backward else 0)
+        self.joint = w.Nt > 0
+        if self.joint:
+            # text tokens replicated on every virtual rank: q_txt, k_txt, v_txt [B, H, Nt, D]
+            self.host.update({n: t.pin_memory() for n, t in wl.make_text_inputs(w).items()})
+            for n in ("q_txt", "k_txt", "v_txt"):
+                self.dev[n] = self.host[n].cuda()
+            tshape, lshape = (w.B, w.H, w.Nt, w.D), (w.B, w.H, w.Nt)
+            self.txt_out = {m: (torch.empty(tshape, dtype=w.torch_dtype, device="cuda"),
+                                torch.empty(lshape, dtype=torch.float32, device="cuda")) for m in ("m", "f")}
+            nws = usp.joint_workspace_bytes(w.B, w.H, w.N, w.Nt, w.D, w.ulysses, w.ring, w.torch_dtype,
+                                            "materialised", True)
+            self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+            # materialised: tok2head, partials against the image chunks, partials against the text,
+            # merge, head2tok x2, text merge; fused: one launch (image and text queries)
+            self.launches_per_step = 7 + 1
 
     def flop(self):
+        if self.joint:
+            return 2 * self.w.joint_flop(True)
         f = 2 * self.w.fwd_flop
         if self.backward:
             f += self.w.bwd_flop
         return f
+
+    def fwd(self, mode):
+        """One forward call of the step (joint when the workload has text tokens)."""
+        usp, w, d = self.usp, self.w, self.dev
+        out, lse = (self.out_m, self.lse_m) if mode == "materialised" else (self.out_f, self.lse_f)
+        ws = self.ws if mode == "materialised" else None
+        if not self.joint:
+            usp.attention_fwd(d["q"], d["k"], d["v"], w.ulysses, w.ring, w.scale, mode=mode, out=out, lse=lse,
+                              workspace=ws)
+            return
+        from diffusion_transformer_sequence_gb300 import _lib
+        ot, lt = self.txt_out[mode[0]]
+        rc = usp.lib().usp_attention_fwd_joint(
+            d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(), d["q_txt"].data_ptr(), d["k_txt"].data_ptr(),
+            d["v_txt"].data_ptr(), out.data_ptr(), lse.data_ptr(), ot.data_ptr(), lt.data_ptr(), w.B, w.H, w.N,
+            w.Nt, w.D, w.ulysses, w.ring, w.scale, _lib.USP_BF16 if w.dtype == "bf16" else _lib.USP_F32,
+            _lib.USP_MATERIALISED if mode == "materialised" else _lib.USP_FUSED,
+            ws.data_ptr() if ws is not None else None, ws.numel() if ws is not None else 0,
+            torch.cuda.current_stream().cuda_stream)
+        _lib.check("usp_attention_fwd_joint", rc)
 
     def flush(self):
         self.flush_buf.fill_(1)
@@ -251,13 +301,11 @@ class Step:
         if ev:
             ev[0].record()
         if only in (None, "materialised"):
-            usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
-                              mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
+            self.fwd("materialised")
         if ev:
             ev[1].record()
         if only in (None, "fused"):
-            usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
-                              mode="fused", out=self.out_f, lse=self.lse_f)
+            self.fwd("fused")
         if ev:
             ev[2].record()
         if self.backward and only in (None, "backward"):
@@ -280,13 +328,15 @@ class Step:
     def run_e2e(self):
         """Host buffers in and out: H2D of q, k, v, the step, D2H of the outputs."""
         usp, w = self.usp, self.w
-        for n in ("q", "k", "v"):
-            self.dev[n].copy_(self.host[n], non_blocking=True)
-        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
-                          mode="materialised", out=self.out_m, lse=self.lse_m, workspace=self.ws)
-        usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
-                          mode="fused", out=self.out_f, lse=self.lse_f)
+        for n in self.inputs():
+            if n != "dout":
+                self.dev[n].copy_(self.host[n], non_blocking=True)
+        self.fwd("materialised")
+        self.fwd("fused")
         outs = [("out_m", self.out_m), ("lse_m", self.lse_m), ("out_f", self.out_f), ("lse_f", self.lse_f)]
+        if self.joint:
+            outs += [("ot_m", self.txt_out["m"][0]), ("lt_m", self.txt_out["m"][1]),
+                     ("ot_f", self.txt_out["f"][0]), ("lt_f", self.txt_out["f"][1])]
         if self.backward:
             self.dev["dout"].copy_(self.host["dout"], non_blocking=True)
             self.bwd()
@@ -298,10 +348,15 @@ class Step:
                 setattr(self, "h_" + name, dst)
             dst.copy_(t, non_blocking=True)
 
+    def inputs(self):
+        names = ["q", "k", "v"] + (["dout"] if self.backward else [])
+        return names + (["q_txt", "k_txt", "v_txt"] if self.joint else [])
+
     def io_bytes(self):
-        names = ("q", "k", "v", "dout") if self.backward else ("q", "k", "v")
-        h2d = sum(self.host[n].numel() * self.host[n].element_size() for n in names)
+        h2d = sum(self.host[n].numel() * self.host[n].element_size() for n in self.inputs())
         d2h = 2 * (self.out_m.numel() * self.out_m.element_size() + self.lse_m.numel() * 4)
+        if self.joint:
+            d2h += 2 * sum(t.numel() * t.element_size() for t in self.txt_out["m"])
         if self.backward:
             d2h += sum(g.numel() * g.element_size() for g in self.grads)
         return h2d, d2h
@@ -348,6 +403,17 @@ def time_rows(w, reps=10):
     T = torch.empty_like(q)
     t = timed(lambda: usp.relayout_head2tok(X, w.ulysses, w.ring, out=T))
     res["head2tok"] = {"GB/s": 2 * w.t_bytes / t / 1e9, "us": t * 1e6, "bytes": 2 * w.t_bytes}
+    if w.Nt:
+        # cross-attention of the sharded image queries to the replicated text K/V (tensor-bound:
+        # reported as TFLOP/s beside its bytes)
+        kt = torch.randn((w.B, w.H, w.Nt, w.D), device="cuda").to(w.torch_dtype)
+        vt = torch.randn((w.B, w.H, w.Nt, w.D), device="cuda").to(w.torch_dtype)
+        o = torch.empty_like(q)
+        l = torch.empty(w.lse_stack_shape, device="cuda")
+        t = timed(lambda: usp.cross_attention_fwd(q, kt, vt, w.ulysses, w.ring, w.scale, out=o, lse=l))
+        flop = 4.0 * w.B * w.H * w.N * w.Nt * w.D
+        byt = 2 * w.t_bytes + w.B * w.H * w.N * 4 + 2 * kt.numel() * kt.element_size()
+        res["cross_attention"] = {"GB/s": byt / t / 1e9, "us": t * 1e6, "bytes": byt, "TFLOP/s": flop / t / 1e12}
     if w.ring > 1:
         R = w.ring
         outs = torch.randn((R, w.B, w.H, w.N, w.D), device="cuda").to(w.torch_dtype)
@@ -365,7 +431,7 @@ def our_arm(args, w, ws, rank, local):
     import diffusion_transformer_sequence_gb300 as usp
     usp.lib()
     peaks = load_peaks()
-    step = Step(w, backward=not args.no_backward)
+    step = Step(w, backward=not args.no_backward and not w.Nt)   # the joint path is forward-only
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     L = usp.lib()
     import ctypes
@@ -426,10 +492,14 @@ def our_arm(args, w, ws, rank, local):
         return
     fused_s = statistics.mean(fus)
     mat_s = statistics.mean(mat)
-    fused_tflops = w.fwd_flop / fused_s / 1e12
+    fwd_flop = w.joint_flop(True) if step.joint else w.fwd_flop
+    fused_tflops = fwd_flop / fused_s / 1e12
     peak = peaks["bf16_tflops"]
     # the dominant kernel of the step: the one with the largest device time per step
     kernels = {"attn_tc_fwd_kernel": (fused_s, w.fwd_flop, "fused USP forward (one launch per call)")}
+    if step.joint:
+        kernels = {"attn_tc_fwd_kernel": (fused_s, fwd_flop,
+                                          "fused joint forward (image and text queries, one launch per call)")}
     if bwd_phases and len(bwd_phases[0]) == 3:
         dkdv_s = statistics.mean(p[1] for p in bwd_phases)
         dq_s = statistics.mean(p[2] for p in bwd_phases)
@@ -460,16 +530,20 @@ def our_arm(args, w, ws, rank, local):
         "config": {"workload": w.name, "desc": w.description, "global_batch": w.B * ws, "seq_len": w.N,
                    "heads": w.H, "head_dim": w.D, "ulysses": w.ulysses, "ring": w.ring,
                    "parallelism": f"{ws} independent replicas; u x r virtual ranks per device",
-                   "step": "usp_attention_fwd materialised + usp_attention_fwd fused"
-                           + (" + usp_attention_bwd" if step.backward else ""),
+                   **({"text_len": w.Nt} if step.joint else {}),
+                   "step": ("usp_attention_fwd_joint materialised + usp_attention_fwd_joint fused (with text queries)"
+                            if step.joint else
+                            "usp_attention_fwd materialised + usp_attention_fwd fused"
+                            + (" + usp_attention_bwd" if step.backward else "")),
                    "l2": "flushed (256 MB write) before every timed step, outside the events"},
         "rows": {"materialised_fwd_ms": mat_s * 1e3, "fused_fwd_ms": fused_s * 1e3,
-                 "materialised_fwd_tflops": w.fwd_flop / mat_s / 1e12, "fused_fwd_tflops": fused_tflops,
+                 "materialised_fwd_tflops": fwd_flop / mat_s / 1e12, "fused_fwd_tflops": fused_tflops,
                  **({"bwd_ms": statistics.mean(bwd) * 1e3,
                      "bwd_tflops": w.bwd_flop / statistics.mean(bwd) / 1e12} if step.backward else {}),
                  **({k + "_ms": v[0] * 1e3 for k, v in kernels.items()}),
                  **({k + "_tflops": v[1] / v[0] / 1e12 for k, v in kernels.items()}),
                  **{k + "_GBps": v["GB/s"] for k, v in rows.items()},
+                 **{k + "_tflops": v["TFLOP/s"] for k, v in rows.items() if "TFLOP/s" in v},
                  **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items()}},
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -492,7 +566,7 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
-    ap.add_argument("--workload", default="qwen1024", choices=wl.ORDER)
+    ap.add_argument("--workload", default="qwen1024", choices=wl.ORDER + wl.JOINT)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row GB/s timings")

@@ -6,8 +6,11 @@ The compute path lives in ``libusp.so`` (``csrc/``, declared in
 from .api import (  # noqa: F401
     attention_bwd,
     attention_fwd,
+    attention_fwd_joint,
     attn_chunk_fwd,
+    cross_attention_fwd,
     device_status,
+    joint_workspace_bytes,
     lse_merge,
     relayout_head2tok,
     relayout_tok2head,

@@ -156,6 +156,79 @@ def attention_fwd(q, k, v, ulysses: int, ring: int, scale: float | None = None, 
     return out, lse
 
 
+def joint_workspace_bytes(B, H, N, Nt, D, ulysses, ring, dtype=torch.bfloat16, mode="fused",
+                          text_queries=True) -> int:
+    return int(_lib.lib().usp_attention_joint_workspace_bytes(B, H, N, Nt, D, ulysses, ring, _DT[dtype],
+                                                              _MODES[mode], 1 if text_queries else 0))
+
+
+def attention_fwd_joint(q, k, v, k_txt, v_txt, ulysses: int, ring: int, scale: float | None = None,
+                        q_txt=None, mode: str = "fused", workspace=None):
+    """Joint text + image USP attention forward.
+
+    q, k, v: token-sharded image stacks [ring, ulysses, B, H, Ns, D];
+    k_txt, v_txt (and q_txt): replicated text tensors [B, H, Nt, D].
+    Returns (out, lse) in the stack layout and, when q_txt is given,
+    (out_txt [B, H, Nt, D], lse_txt [B, H, Nt]).  CPU inputs take the host
+    path of :func:`attention_fwd`.
+    """
+    host = not q.is_cuda
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        q, k, v, k_txt, v_txt = _to_device((q, k, v, k_txt, v_txt), dev)
+        if q_txt is not None:
+            (q_txt,) = _to_device((q_txt,), dev)
+    B, H, N, D = _stack_dims(q, ulysses, ring)
+    Nt = k_txt.shape[2]
+    for t in (k_txt, v_txt) + (() if q_txt is None else (q_txt,)):
+        if tuple(t.shape) != (B, H, Nt, D) or t.dtype != q.dtype:
+            raise ValueError("text tensors must be [B, H, Nt, D] in the image dtype")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:5], dtype=torch.float32, device=q.device)
+    out_txt = lse_txt = None
+    if q_txt is not None:
+        out_txt = torch.empty_like(q_txt)
+        lse_txt = torch.empty((B, H, Nt), dtype=torch.float32, device=q.device)
+    _dev(*[t for t in (q, k, v, k_txt, v_txt, q_txt, out, lse, out_txt, lse_txt) if t is not None])
+    need = joint_workspace_bytes(B, H, N, Nt, D, ulysses, ring, q.dtype, mode, q_txt is not None)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    check("usp_attention_fwd_joint", _lib.lib().usp_attention_fwd_joint(
+        _p(q), _p(k), _p(v), _p(q_txt), _p(k_txt), _p(v_txt), _p(out), _p(lse), _p(out_txt), _p(lse_txt),
+        B, H, N, Nt, D, ulysses, ring, scale, _dt(q), _MODES[mode], _p(workspace) if need else None, need,
+        _stream()))
+    res = (out, lse) if q_txt is None else (out, lse, out_txt, lse_txt)
+    if host:
+        res = tuple(_to_host(t) for t in res)
+        torch.cuda.current_stream().synchronize()
+    return res
+
+
+def cross_attention_fwd(q, k_txt, v_txt, ulysses: int, ring: int, scale: float | None = None, out=None, lse=None):
+    """Cross-attention of the token-sharded image queries [ring, ulysses, B, H,
+    Ns, D] to the replicated text K/V [B, H, Nt, D] -> (out, lse) in the
+    stack layout.  CPU inputs take the host path of :func:`attention_fwd`."""
+    host = not q.is_cuda
+    if host:
+        q, k_txt, v_txt = _to_device((q, k_txt, v_txt), torch.device("cuda", torch.cuda.current_device()))
+    B, H, N, D = _stack_dims(q, ulysses, ring)
+    Nt = k_txt.shape[2]
+    for t in (k_txt, v_txt):
+        if tuple(t.shape) != (B, H, Nt, D) or t.dtype != q.dtype:
+            raise ValueError("text K/V must be [B, H, Nt, D] in the query dtype")
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:5], dtype=torch.float32, device=q.device) if lse is None else lse
+    _dev(q, k_txt, v_txt, out, lse)
+    check("usp_cross_attention_fwd", _lib.lib().usp_cross_attention_fwd(
+        _p(q), _p(k_txt), _p(v_txt), _p(out), _p(lse), B, H, N, Nt, D, ulysses, ring, scale, _dt(q), _stream()))
+    if host:
+        out, lse = _to_host(out), _to_host(lse)
+        torch.cuda.current_stream().synchronize()
+    return out, lse
+
+
 def attention_bwd(q, k, v, out, lse, dout, ulysses: int, ring: int, scale: float | None = None,
                   workspace=None):
     """USP attention backward over token-sharded stacks -> (dq, dk, dv)."""

@@ -6,13 +6,12 @@
 // warp-shuffle reductions (online softmax), and each lane accumulates the
 // output dimensions d = lane + 32*i.  All arithmetic is IEEE fp32 with expf.
 //
-// Addressing modes:
-//  * plain / materialised: heads are contiguous [rows][D] blocks; a "unit"
-//    (one query head against one KV head) is mapped through the ring
-//    schedule: unit = (t, g, j, b, h') -> KV chunk c = (g - t) mod ring, and
-//    the output of ring step t goes to head t*out_step_stride + q_head.
-//  * fused: q/k/v/out are the token-sharded stack [sp][BH][Ns][D]; a unit is
-//    one (b, h) head attending over every shard's keys.
+// Addressing: each operand is either plain [heads][rows][D] or the
+// token-sharded stack [sp][BH][Ns][D] (sp*Ns rows per head); a unit (one
+// query head against one KV head) is mapped to heads by the UnitMap (plain,
+// materialised ring step, image-vs-text, text-vs-image chunk).  An optional
+// second KV source (plain; the text tokens of joint attention) follows the
+// first source's keys in the same online softmax.
 #include "usp_internal.cuh"
 
 namespace usp {
@@ -36,37 +35,51 @@ struct F32Addr {
   }
 };
 
+// One operand of the forward: plain [heads][rows][D] or the token-sharded
+// stack [sp][BH][Ns][D] read as sp*Ns rows per head.
+struct F32Operand {
+  const float* k;
+  const float* v;
+  bool stack;
+  int64_t rows;  // rows per head
+  __device__ __forceinline__ int64_t off(int64_t head, int64_t row, int D, const F32Addr& st) const {
+    return stack ? st.row_off(head, row, 0, D) : (head * rows + row) * (int64_t)D;
+  }
+};
+
+struct F32Fwd {
+  const float* q;
+  float* out;
+  float* lse;
+  bool q_stack;  // out follows q
+  int64_t Nq;
+  F32Operand kv, kv2;  // kv2.rows == 0: no second source
+  F32Addr stack;
+  UnitMap map;
+  float scale;
+};
+
 template <int kDmax>
-__global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(
-    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
-    float* __restrict__ out, float* __restrict__ lse, int64_t Nq, int64_t Nk, int D, float scale,
-    RingSchedule sched, int64_t out_step_stride, F32Addr addr) {
+__global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(const F32Fwd p, int D) {
   __shared__ float Ks[kTileK][kDmax + 1];
   __shared__ float Vs[kTileK][kDmax];
   __shared__ float Qs[kWarps][kDmax];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  // unit -> (q head, kv head, out head)
-  const int64_t unit = blockIdx.y;
-  const int64_t per_step = (int64_t)sched.ring * sched.ulysses * sched.heads_per_rank;
-  const int64_t t = unit / per_step;
-  const int64_t qh = unit - t * per_step;
-  const int64_t rank_stride = (int64_t)sched.heads_per_rank;        // heads per virtual rank
-  const int64_t g = qh / (rank_stride * sched.ulysses);
-  const int64_t c = ((g - t) % sched.ring + sched.ring) % sched.ring;
-  const int64_t kvh = qh + (c - g) * rank_stride * sched.ulysses;
-  const int64_t oh = t * out_step_stride + qh;
+  const UnitHeads U = map_unit(p.map, blockIdx.y);
+  const F32Operand qop{p.q, nullptr, p.q_stack, p.Nq};
 
   const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
-  const bool active = row < Nq;
+  const bool active = row < p.Nq;
   if (active)
-    for (int d = lane; d < D; d += 32) Qs[warp][d] = q[addr.row_off(qh, row, Nq, D) + d];
+    for (int d = lane; d < D; d += 32) Qs[warp][d] = p.q[qop.off(U.qh, row, D, p.stack) + d];
 
   float m = -INFINITY, l = 0.f;
   float o[kDmax / 32];
 #pragma unroll
   for (int i = 0; i < kDmax / 32; ++i) o[i] = 0.f;
 
+  const int64_t n1 = p.kv.rows, Nk = n1 + p.kv2.rows;  // keys: first source, then second
   for (int64_t j0 = 0; j0 < Nk; j0 += kTileK) {
     __syncthreads();
     const int nk = (int)((Nk - j0) < kTileK ? (Nk - j0) : kTileK);
@@ -74,9 +87,12 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(
       const int jj = e / D, d = e - jj * D;
       float kv = 0.f, vv = 0.f;
       if (jj < nk) {
-        const int64_t off = addr.row_off(kvh, j0 + jj, Nk, D) + d;
-        kv = k[off];
-        vv = v[off];
+        const int64_t key = j0 + jj;
+        const bool second = key >= n1;
+        const F32Operand& src = second ? p.kv2 : p.kv;
+        const int64_t off = src.off(second ? U.kvh2 : U.kvh, second ? key - n1 : key, D, p.stack) + d;
+        kv = src.k[off];
+        vv = src.v[off];
       }
       Ks[jj][d] = kv;
       Vs[jj][d] = vv;
@@ -87,22 +103,22 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(
     if (lane < nk) {
       float acc = 0.f;
       for (int d = 0; d < D; ++d) acc = fmaf(Qs[warp][d], Ks[lane][d], acc);
-      s = acc * scale;
+      s = acc * p.scale;
     }
     float mx = s;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
     const float m_new = fmaxf(m, mx);
-    const float p = (lane < nk) ? expf(s - m_new) : 0.f;
+    const float pr = (lane < nk) ? expf(s - m_new) : 0.f;
     const float alpha = expf(m - m_new);  // m = -inf on the first tile -> 0
-    float ps = p;
+    float ps = pr;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
     l = l * alpha + ps;
 #pragma unroll
     for (int i = 0; i < kDmax / 32; ++i) o[i] *= alpha;
     for (int jj = 0; jj < nk; ++jj) {
-      const float pj = __shfl_sync(0xffffffffu, p, jj);
+      const float pj = __shfl_sync(0xffffffffu, pr, jj);
 #pragma unroll
       for (int i = 0; i < kDmax / 32; ++i) {
         const int d = lane + 32 * i;
@@ -113,31 +129,13 @@ __global__ void __launch_bounds__(kWarps * 32) attn_f32_kernel(
   }
   if (!active) return;
   const float inv = 1.f / l;
-  const int64_t ooff = addr.row_off(oh, row, Nq, D);
+  const int64_t ooff = qop.off(U.oh, row, D, p.stack);
 #pragma unroll
   for (int i = 0; i < kDmax / 32; ++i) {
     const int d = lane + 32 * i;
-    if (d < D) out[ooff + d] = o[i] * inv;
+    if (d < D) p.out[ooff + d] = o[i] * inv;
   }
-  if (lane == 0) lse[addr.lse_off(oh, row, Nq)] = m + logf(l);
-}
-
-template <int kDmax>
-cudaError_t launch_dmax(const float* q, const float* k, const float* v, float* out, float* lse,
-                        int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
-                        int64_t out_step_stride, F32Addr addr, int64_t units, cudaStream_t stream) {
-  dim3 grid((unsigned)((Nq + kWarps - 1) / kWarps), (unsigned)units, 1);
-  attn_f32_kernel<kDmax><<<grid, kWarps * 32, 0, stream>>>(q, k, v, out, lse, Nq, Nk, D, scale, sched,
-                                                           out_step_stride, addr);
-  return cudaGetLastError();
-}
-
-cudaError_t dispatch(const float* q, const float* k, const float* v, float* out, float* lse,
-                     int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
-                     int64_t out_step_stride, F32Addr addr, int64_t units, cudaStream_t stream) {
-  if (D <= 32) return launch_dmax<32>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
-  if (D <= 64) return launch_dmax<64>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
-  return launch_dmax<128>(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride, addr, units, stream);
+  if (lane == 0) p.lse[ooff / D] = m + logf(l);
 }
 
 // ---------------------------------------------------------------- backward
@@ -275,21 +273,29 @@ cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, 
   return launch_bwd_dmax<128>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
 }
 
-cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* out, float* lse,
-                            int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
-                            int64_t out_step_stride_heads, cudaStream_t stream) {
-  const int64_t units = (int64_t)sched.steps * sched.ring * sched.ulysses * sched.heads_per_rank;
-  F32Addr addr{false, 0, 0};
-  return dispatch(q, k, v, out, lse, Nq, Nk, D, scale, sched, out_step_stride_heads, addr, units, stream);
-}
-
-cudaError_t launch_attn_f32_fused(const float* q, const float* k, const float* v, float* out,
-                                  float* lse, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
-                                  cudaStream_t stream) {
-  RingSchedule sched{1, 1, 1, (int)BH};
-  F32Addr addr{true, BH, Ns};
-  const int64_t N = sp * Ns;
-  return dispatch(q, k, v, out, lse, N, N, D, scale, sched, 0, addr, BH, stream);
+cudaError_t launch_attn_f32(const AttnArgs& a, int D, cudaStream_t stream) {
+  if (a.out_stack != a.q_stack) return cudaErrorInvalidValue;  // out rows follow the query rows
+  F32Fwd p{};
+  p.q = static_cast<const float*>(a.q);
+  p.out = static_cast<float*>(a.out);
+  p.lse = a.lse;
+  p.q_stack = a.q_stack;
+  p.Nq = a.q_stack ? a.sp * a.Ns : a.Nq;
+  p.kv = F32Operand{static_cast<const float*>(a.k), static_cast<const float*>(a.v), a.kv_stack,
+                    a.kv_stack ? a.sp * a.Ns : a.Nk};
+  p.kv2 = F32Operand{static_cast<const float*>(a.k2), static_cast<const float*>(a.v2), false,
+                     a.k2 ? a.Nk2 : 0};
+  p.stack = F32Addr{true, a.BH, a.Ns};
+  p.map = a.map;
+  p.scale = a.scale;
+  dim3 grid((unsigned)((p.Nq + kWarps - 1) / kWarps), (unsigned)a.units, 1);
+  if (D <= 32)
+    attn_f32_kernel<32><<<grid, kWarps * 32, 0, stream>>>(p, D);
+  else if (D <= 64)
+    attn_f32_kernel<64><<<grid, kWarps * 32, 0, stream>>>(p, D);
+  else
+    attn_f32_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p, D);
+  return cudaGetLastError();
 }
 
 }  // namespace usp

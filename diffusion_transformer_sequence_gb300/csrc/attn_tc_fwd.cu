@@ -64,46 +64,56 @@ constexpr int B_MMADONE = B_ODONE + 2;
 constexpr int NUM_BARS = B_MMADONE + 1;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_SLOT + 8;
-constexpr int SMEM_USED = OFF_ABORT + 8;
+constexpr int OFF_EPI = OFF_ABORT + 8;        // EpiInfo (written once by thread 0)
+constexpr int SMEM_USED = OFF_EPI + 48;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment of the base
 
-struct TcParams {
+// How the 128-row tiles of one operand are addressed.
+//   kind 0: 3-D tensor map (D, rows, heads), tiles 0.. of one head
+//   kind 1: 4-D tensor map over the token-sharded stack (D, Ns, B*H, sp);
+//           tile t is tile (t % tps) of shard (t / tps)
+struct TileSrc {
+  int kind;
+  int64_t rows;  // kind 0: rows per head; kind 1: Ns
+  int tps;       // tiles per head (kind 0) or per shard (kind 1)
+  int tiles;     // tiles in total
+};
+
+// One query set of a launch and where its results go.
+struct QSide {
+  TileSrc q;
   void* out;
   float* lse;
-  int64_t Nq, Nk;           // rows per head (plain addressing)
-  RingSchedule sched;
-  int64_t out_step_stride;  // heads between ring steps in out / lse
-  int fused;
-  int64_t BH, Ns;           // fused addressing
-  int q_tiles;              // query tiles per unit
-  int kv_tiles;             // KV tiles per unit
-  int tiles_per_seg;        // fused: tiles per shard
+  int out_kind;             // 0: out row = oh * out_rows + row;  1: token-sharded stack
+  int64_t out_rows;
+  UnitMap map;
+  int pairs;                // CTAs per unit (pairs of query tiles)
+  int64_t ctas;             // pairs * units
+};
+
+// A launch serves one or two query sets over the same KV sources: CTAs
+// [0, qs[0].ctas) the first set, the rest the second (e.g. the image and the
+// text queries of joint attention), so a short second set fills the first
+// one's last wave instead of running as a launch of its own.
+struct TcParams {
+  QSide qs[2];
+  TileSrc kv, kv2;          // kv2: optional second KV source (kind 0), e.g. text tokens
+  int64_t BH, Ns;           // token-sharded stack geometry
   float scale_log2;         // scale * log2(e)
   Guard guard;
 };
 
-struct Unit {
-  int64_t qh, kvh, oh;
+// Where the epilogue of each query tile of the CTA writes: its first output
+// row, how many rows exist, and the out / lse base pointers.  Warp 2 (idle
+// otherwise) fills it before the CTA's first barrier, so the softmax warps
+// carry none of the query set's parameters through the KV loop.
+struct EpiInfo {
+  int64_t orow0[2];
+  void* out;
+  float* lse;
+  int valid[2];
 };
-
-__device__ __forceinline__ Unit unit_heads(const TcParams& p, int64_t unit) {
-  Unit u;
-  if (p.fused) {
-    u.qh = u.kvh = u.oh = unit;
-    return u;
-  }
-  const RingSchedule& s = p.sched;
-  const int64_t per_step = (int64_t)s.ring * s.ulysses * s.heads_per_rank;
-  const int64_t t = unit / per_step;
-  const int64_t qh = unit - t * per_step;
-  const int64_t rank_heads = (int64_t)s.heads_per_rank * s.ulysses;  // heads per ring group
-  const int64_t g = qh / rank_heads;
-  const int64_t c = ((g - t) % s.ring + s.ring) % s.ring;             // KV chunk at ring step t
-  u.qh = qh;
-  u.kvh = qh + (c - g) * rank_heads;
-  u.oh = t * p.out_step_stride + qh;
-  return u;
-}
+static_assert(sizeof(EpiInfo) <= 48, "EpiInfo slot");
 
 // A tile of a head: its first row inside its shard (or head), the shard, and
 // how many of its 128 rows exist.
@@ -112,25 +122,24 @@ struct TileRef {
   int seg;
   int valid;
 };
-__device__ __forceinline__ TileRef tile_ref(const TcParams& p, int tile, bool is_q) {
+__device__ __forceinline__ TileRef tile_of(const TileSrc& src, int tile) {
   TileRef t;
-  if (p.fused) {
-    t.seg = tile / p.tiles_per_seg;
-    t.row0 = (tile - t.seg * p.tiles_per_seg) * BM;
-    const int64_t rem = p.Ns - t.row0;
-    t.valid = rem < BM ? (int)rem : BM;
-  } else {
-    t.seg = 0;
-    t.row0 = tile * BM;
-    const int64_t rem = (is_q ? p.Nq : p.Nk) - t.row0;
-    t.valid = rem < BM ? (int)rem : BM;
-  }
+  t.seg = src.kind == 1 ? tile / src.tps : 0;
+  t.row0 = (tile - t.seg * src.tps) * BM;
+  const int64_t rem = src.rows - t.row0;
+  t.valid = rem < BM ? (int)rem : BM;
   return t;
 }
+// KV tile j of a CTA: the first source's tiles, then the second source's.
+template <bool kKv2>
+__device__ __forceinline__ TileRef kv_tile(const TileSrc& kv, const TileSrc& kv2, int j, bool& second) {
+  second = kKv2 && j >= kv.tiles;
+  return second ? tile_of(kv2, j - kv.tiles) : tile_of(kv, j);
+}
 
-__device__ __forceinline__ void load_tile(const CUtensorMap* map, const TcParams& p, uint32_t dst,
-                                          uint32_t bar, int64_t head, const TileRef& t) {
-  if (p.fused) {
+__device__ __forceinline__ void load_tile(const CUtensorMap* map, int kind, uint32_t dst, uint32_t bar,
+                                          int64_t head, const TileRef& t) {
+  if (kind == 1) {
     ptx::tma_load_4d(dst, map, bar, 0, t.row0, (int)head, t.seg);
     ptx::tma_load_4d(dst + HALF_BYTES, map, bar, 64, t.row0, (int)head, t.seg);
   } else {
@@ -144,9 +153,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// kKv2: a second KV source follows the first (compiled out when absent).
+template <bool kKv2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    attn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+    attn_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
+                       const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v2,
+                       const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = ptx::smem_u32(smem);
@@ -156,10 +169,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int64_t unit = blockIdx.y;
-  const Unit U = unit_heads(p, unit);
-  const int qt0 = 2 * blockIdx.x;
-  const int qt1 = (qt0 + 1 < p.q_tiles) ? qt0 + 1 : -1;  // -1: no second tile (compute on a copy)
+  // query set, unit and query-tile pair of this CTA
+  const int side = (int64_t)blockIdx.x >= p.qs[0].ctas ? 1 : 0;
+  const int local = (int)blockIdx.x - (side ? (int)p.qs[0].ctas : 0);  // the grid has < 2^31 CTAs
+  const int pairs = side ? p.qs[1].pairs : p.qs[0].pairs;
+  const int q_tiles = side ? p.qs[1].q.tiles : p.qs[0].q.tiles;
+  const int unit = local / pairs;
+  const int qt0 = 2 * (int)(local - unit * pairs);
+  const int qt1 = (qt0 + 1 < q_tiles) ? qt0 + 1 : -1;  // -1: no second tile (compute on a copy)
+  const int kv_total = kKv2 ? p.kv.tiles + p.kv2.tiles : p.kv.tiles;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B_QFULL), 1);
@@ -179,14 +197,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
+  if (warp == 2 && lane == 0) {  // an otherwise idle warp fills the epilogue's addressing
+    {
+      const QSide& S = p.qs[side];
+      const int64_t oh = map_unit(S.map, unit).oh;
+      EpiInfo* epi = reinterpret_cast<EpiInfo*>(smem + OFF_EPI);
+      for (int i = 0; i < 2; ++i) {
+        const int qt = i == 0 ? qt0 : qt1;
+        const TileRef t = tile_of(S.q, qt >= 0 ? qt : qt0);
+        epi->orow0[i] = S.out_kind == 1 ? ((int64_t)t.seg * p.BH + oh) * p.Ns + t.row0 : oh * S.out_rows + t.row0;
+        epi->valid[i] = qt >= 0 ? t.valid : 0;
+      }
+      epi->out = S.out;
+      epi->lse = S.lse;
+    }
+  }
   if (warp == 1) {
     ptx::tmem_alloc(sbase + OFF_SLOT, 512);
     ptx::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(side ? &tm_q1 : &tm_q0);
     ptx::prefetch_tmap(&tm_k);
     ptx::prefetch_tmap(&tm_v);
+    if (kKv2) {
+      ptx::prefetch_tmap(&tm_k2);
+      ptx::prefetch_tmap(&tm_v2);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -203,23 +240,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const TileRef q0 = tile_ref(p, qt0, true);
-      const TileRef q1 = tile_ref(p, qt1 >= 0 ? qt1 : qt0, true);
+      const QSide& S = p.qs[side];
+      const UnitHeads U = map_unit(S.map, unit);
+      const TileRef q0 = tile_of(S.q, qt0);
+      const TileRef q1 = tile_of(S.q, qt1 >= 0 ? qt1 : qt0);
       ptx::mbar_arrive_expect_tx(bar(B_QFULL), 2 * TILE_BYTES);
-      load_tile(&tm_q, p, sbase + OFF_Q, bar(B_QFULL), U.qh, q0);
-      load_tile(&tm_q, p, sbase + OFF_Q + TILE_BYTES, bar(B_QFULL), U.qh, q1);
+      const CUtensorMap* mq = side ? &tm_q1 : &tm_q0;
+      load_tile(mq, S.q.kind, sbase + OFF_Q, bar(B_QFULL), U.qh, q0);
+      load_tile(mq, S.q.kind, sbase + OFF_Q + TILE_BYTES, bar(B_QFULL), U.qh, q1);
       int issued_k = 0, issued_v = 0;
-      for (int j = 0; j < p.kv_tiles; ++j) {
+      for (int j = 0; j < kv_total; ++j) {
         const int s = j % KV_STAGES;
         const uint32_t ph = (uint32_t)((j / KV_STAGES) & 1);
-        const TileRef kt = tile_ref(p, j, false);
+        bool second;
+        const TileRef kt = kv_tile<kKv2>(p.kv, p.kv2, j, second);
+        const CUtensorMap* mk = second ? &tm_k2 : &tm_k;
+        const CUtensorMap* mv = second ? &tm_v2 : &tm_v;
+        const int kind = second ? 0 : p.kv.kind;
+        const int64_t head = second ? U.kvh2 : U.kvh;
         if (!ptx::mbar_wait(bar(B_KEMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
         ptx::mbar_arrive_expect_tx(bar(B_KFULL + s), TILE_BYTES);
-        load_tile(&tm_k, p, sbase + OFF_K + s * TILE_BYTES, bar(B_KFULL + s), U.kvh, kt);
+        load_tile(mk, kind, sbase + OFF_K + s * TILE_BYTES, bar(B_KFULL + s), head, kt);
         issued_k = j + 1;
         if (!ptx::mbar_wait(bar(B_VEMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
         ptx::mbar_arrive_expect_tx(bar(B_VFULL + s), TILE_BYTES);
-        load_tile(&tm_v, p, sbase + OFF_V + s * TILE_BYTES, bar(B_VFULL + s), U.kvh, kt);
+        load_tile(mv, kind, sbase + OFF_V + s * TILE_BYTES, bar(B_VFULL + s), head, kt);
         issued_v = j + 1;
       }
       // Drain: every copy this thread issued must land before shared memory is released.
@@ -265,7 +310,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::mma_ss(tS[i], dq + off, dk + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
-      for (int j = 0; ok && j < p.kv_tiles; ++j) {
+      for (int j = 0; ok && j < kv_total; ++j) {
         const int s = j % KV_STAGES;
         if (!(ok = ptx::mbar_wait(bar(B_KFULL + s), (uint32_t)((j / KV_STAGES) & 1), G, abort_flag, kDevTimeoutMma))) break;
         ptx::tc_fence_after();
@@ -287,7 +332,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mma_commit(bar(B_KEMPTY + s));
       }
       if (ok) {
-        const int jl = p.kv_tiles - 1;
+        const int jl = kv_total - 1;
         for (int i = 0; i < 2 && ok; ++i) {
           if (!(ok = ptx::mbar_wait(bar(B_PFULL + i), (uint32_t)(jl & 1), G, abort_flag, kDevTimeoutMma))) break;
           if (i == 0 && !(ok = ptx::mbar_wait(bar(B_VFULL + jl % KV_STAGES), (uint32_t)((jl / KV_STAGES) & 1), G,
@@ -317,7 +362,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float m = -INFINITY;  // running reference maximum, log2 domain
     float l = 0.f;        // running row sum relative to m
     bool ok = true;
-    for (int j = 0; j < p.kv_tiles; ++j) {
+    for (int j = 0; j < kv_total; ++j) {
       // every lane waits; the decision is made warp-uniform before the
       // warp-collective TMEM accesses below
       ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_SFULL + wg), (uint32_t)(j & 1), G, abort_flag,
@@ -327,7 +372,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t sr[BN];
       ptx::tmem_ld4x32(tS, sr);
       float* s = reinterpret_cast<float*>(sr);
-      const int valid = tile_ref(p, j, false).valid;
+      bool second;
+      const int valid = kv_tile<kKv2>(p.kv, p.kv2, j, second).valid;
       if (valid < BN) {
 #pragma unroll
         for (int c = 0; c < BN; ++c)
@@ -390,16 +436,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(B_ODONE + wg), 0, G, abort_flag, kDevTimeoutEpilogue));
     if (ok) {
       ptx::tc_fence_after();
-      const int qt = wg == 0 ? qt0 : qt1;
-      const TileRef t = tile_ref(p, qt >= 0 ? qt : qt0, true);
-      const bool store = qt >= 0 && row < t.valid;
-      int64_t orow;
-      if (p.fused)
-        orow = ((int64_t)t.seg * p.BH + U.oh) * p.Ns + t.row0 + row;
-      else
-        orow = U.oh * p.Nq + t.row0 + row;
+      const EpiInfo* epi = reinterpret_cast<const EpiInfo*>(smem + OFF_EPI);
+      const bool store = row < epi->valid[wg];
+      const int64_t orow = epi->orow0[wg] + row;
       const float inv_l = 1.f / l;
-      __nv_bfloat16* optr = reinterpret_cast<__nv_bfloat16*>(p.out) + orow * HD;
+      __nv_bfloat16* optr = reinterpret_cast<__nv_bfloat16*>(epi->out) + orow * HD;
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t o[32];
@@ -415,7 +456,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      if (store) p.lse[orow] = (m + log2f(l)) * 0.69314718055994531f;
+      if (store) epi->lse[orow] = (m + log2f(l)) * 0.69314718055994531f;
     }
   }
 
@@ -468,51 +509,101 @@ bool make_map_4d(CUtensorMap* m, const void* base, int64_t Ns, int64_t BH, int64
 
 }  // namespace
 
-cudaError_t launch_attn_tc_fwd(const TcAttnArgs& a, const Guard& g, cudaStream_t stream) {
+namespace {
+
+struct KvMaps {
+  CUtensorMap k, v, k2, v2;
+};
+
+// Query-side description and tensor map of one AttnArgs.
+bool make_qside(const AttnArgs& a, QSide* qs, CUtensorMap* mq) {
+  auto tiles = [](int64_t rows) { return (int)((rows + BM - 1) / BM); };
+  if (a.out_stack != a.q_stack) return false;  // out rows follow the query rows
+  if (a.q_stack) {
+    const int tps = tiles(a.Ns);
+    qs->q = TileSrc{1, a.Ns, tps, (int)(tps * a.sp)};
+    if (!make_map_4d(mq, a.q, a.Ns, a.BH, a.sp)) return false;
+  } else {
+    qs->q = TileSrc{0, a.Nq, tiles(a.Nq), tiles(a.Nq)};
+    if (!make_map_3d(mq, a.q, a.Nq, a.q_heads)) return false;
+  }
+  qs->out = a.out;
+  qs->lse = a.lse;
+  qs->out_kind = a.out_stack ? 1 : 0;
+  qs->out_rows = a.out_stack ? a.Ns : a.Nq;
+  qs->map = a.map;
+  qs->pairs = (qs->q.tiles + 1) / 2;
+  qs->ctas = (int64_t)qs->pairs * a.units;
+  return true;
+}
+
+// KV sources and their tensor maps.
+bool make_kv(const AttnArgs& a, TcParams* p, KvMaps* m) {
+  auto tiles = [](int64_t rows) { return (int)((rows + BM - 1) / BM); };
+  if (a.kv_stack) {
+    const int tps = tiles(a.Ns);
+    p->kv = TileSrc{1, a.Ns, tps, (int)(tps * a.sp)};
+    if (!make_map_4d(&m->k, a.k, a.Ns, a.BH, a.sp) || !make_map_4d(&m->v, a.v, a.Ns, a.BH, a.sp)) return false;
+  } else {
+    p->kv = TileSrc{0, a.Nk, tiles(a.Nk), tiles(a.Nk)};
+    if (!make_map_3d(&m->k, a.k, a.Nk, a.kv_heads) || !make_map_3d(&m->v, a.v, a.Nk, a.kv_heads)) return false;
+  }
+  if (a.k2 && a.Nk2 > 0) {  // second KV source: plain [heads][Nk2][D]
+    p->kv2 = TileSrc{0, a.Nk2, tiles(a.Nk2), tiles(a.Nk2)};
+    if (!make_map_3d(&m->k2, a.k2, a.Nk2, a.kv2_heads) || !make_map_3d(&m->v2, a.v2, a.Nk2, a.kv2_heads))
+      return false;
+  } else {
+    p->kv2 = TileSrc{0, 1, 1, 0};
+    m->k2 = m->k;
+    m->v2 = m->v;
+  }
+  return true;
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc_fwd(const AttnArgs* sides, int nsides, const Guard& g, cudaStream_t stream) {
   static bool attr_set = false;  // per process; the attribute is per function, not per device
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         SMEM_BYTES);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(attn_tc_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  TcParams p{};
-  p.out = a.out;
-  p.lse = a.lse;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.guard = g;
-  CUtensorMap mq, mk, mv;
-  int64_t units;
-  if (a.fused) {
-    const int tps = (int)((a.Ns + BM - 1) / BM);
-    p.fused = 1;
-    p.BH = a.BH;
-    p.Ns = a.Ns;
-    p.tiles_per_seg = tps;
-    p.q_tiles = (int)(tps * a.sp);
-    p.kv_tiles = (int)(tps * a.sp);
-    p.Nq = p.Nk = a.sp * a.Ns;
-    units = a.BH;
-    if (!make_map_4d(&mq, a.q, a.Ns, a.BH, a.sp) || !make_map_4d(&mk, a.k, a.Ns, a.BH, a.sp) ||
-        !make_map_4d(&mv, a.v, a.Ns, a.BH, a.sp))
-      return cudaErrorInvalidValue;
-  } else {
-    p.fused = 0;
-    p.Nq = a.Nq;
-    p.Nk = a.Nk;
-    p.sched = a.sched;
-    p.out_step_stride = a.out_step_stride_heads;
-    p.tiles_per_seg = 0;
-    p.q_tiles = (int)((a.Nq + BM - 1) / BM);
-    p.kv_tiles = (int)((a.Nk + BN - 1) / BN);
-    const int64_t per_step = (int64_t)a.sched.ring * a.sched.ulysses * a.sched.heads_per_rank;
-    units = (int64_t)a.sched.steps * per_step;
-    const int64_t kv_heads = per_step;  // the KV stack holds one step's worth of heads
-    if (!make_map_3d(&mq, a.q, a.Nq, per_step) || !make_map_3d(&mk, a.k, a.Nk, kv_heads) ||
-        !make_map_3d(&mv, a.v, a.Nk, kv_heads))
+  if (nsides < 1 || nsides > 2) return cudaErrorInvalidValue;
+  const AttnArgs& a0 = sides[0];
+  if (nsides == 2) {  // the two query sets share the KV sources, the stack geometry and the scale
+    const AttnArgs& a1 = sides[1];
+    if (a1.k != a0.k || a1.v != a0.v || a1.k2 != a0.k2 || a1.v2 != a0.v2 || a1.kv_stack != a0.kv_stack ||
+        a1.Nk != a0.Nk || a1.Nk2 != a0.Nk2 || a1.kv_heads != a0.kv_heads || a1.kv2_heads != a0.kv2_heads ||
+        a1.BH != a0.BH || a1.Ns != a0.Ns || a1.sp != a0.sp || a1.scale != a0.scale)
       return cudaErrorInvalidValue;
   }
-  dim3 grid((unsigned)((p.q_tiles + 1) / 2), (unsigned)units, 1);
-  attn_tc_fwd_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, p);
+  TcParams p{};
+  CUtensorMap mq[2];
+  KvMaps mkv;
+  for (int i = 0; i < nsides; ++i)
+    if (!make_qside(sides[i], &p.qs[i], &mq[i])) return cudaErrorInvalidValue;
+  if (nsides == 1) {  // an empty second query set
+    p.qs[1] = p.qs[0];
+    p.qs[1].ctas = 0;
+    mq[1] = mq[0];
+  }
+  if (!make_kv(a0, &p, &mkv)) return cudaErrorInvalidValue;
+  p.BH = a0.BH;
+  p.Ns = a0.Ns;
+  p.scale_log2 = a0.scale * 1.4426950408889634f;
+  p.guard = g;
+  const int64_t ctas = p.qs[0].ctas + p.qs[1].ctas;
+  if (ctas < 1 || ctas > 2147483647LL) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)ctas, 1, 1);
+  if (p.kv2.tiles > 0)
+    attn_tc_fwd_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq[0], mq[1], mkv.k, mkv.v, mkv.k2, mkv.v2, p);
+  else
+    attn_tc_fwd_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq[0], mq[1], mkv.k, mkv.v, mkv.k2, mkv.v2,
+                                                                          p);
   return cudaGetLastError();
 }
 

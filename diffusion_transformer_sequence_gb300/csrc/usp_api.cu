@@ -135,6 +135,33 @@ FwdWorkspace fwd_layout(int64_t B, int64_t H, int64_t N, int64_t D, int r, usp_d
   return w;
 }
 
+// Joint (text + image) materialised forward: the image part of fwd_layout
+// with ring + 1 partial planes (the last against the text K/V), plus the
+// text-query partials (ring chunk planes + one text plane) when requested.
+struct JointWorkspace {
+  size_t xq, xk, xv, parts_o, parts_l, xo, xl, tparts_o, tparts_l, total;
+};
+JointWorkspace joint_layout(int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t D, int r, usp_dtype dt,
+                            bool text_queries) {
+  const size_t t = round_up((size_t)(B * H * N * D) * elt_size(dt));
+  const size_t lb = round_up((size_t)(B * H * N) * 4);
+  JointWorkspace w{};
+  size_t off = 0;
+  w.xq = off; off += t;
+  w.xk = off; off += t;
+  w.xv = off; off += t;
+  w.parts_o = off; off += (size_t)(r + 1) * t;
+  w.parts_l = off; off += (size_t)(r + 1) * lb;
+  w.xo = off; off += t;
+  w.xl = off; off += lb;
+  if (text_queries) {
+    w.tparts_o = off; off += (size_t)(r + 1) * round_up((size_t)(B * H * Nt * D) * elt_size(dt));
+    w.tparts_l = off; off += (size_t)(r + 1) * round_up((size_t)(B * H * Nt) * 4);
+  }
+  w.total = off;
+  return w;
+}
+
 int relayout(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_t D, int u, int r,
              int elt, bool tok2head, cudaStream_t s) {
   const int64_t Ns = N / ((int64_t)u * r);
@@ -142,30 +169,69 @@ int relayout(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_
   return e == cudaSuccess ? USP_OK : cuda_fail(e);
 }
 
-// Per-(rank, ring step) chunk attention over the head-sharded stacks.
-int chunk_attention(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B,
-                    int64_t Hu, int64_t Nr, int64_t D, int u, int r, float scale, usp_dtype dt,
-                    cudaStream_t s) {
-  RingSchedule sched{u, r, r, (int)(B * Hu)};
-  const int64_t step_heads = (int64_t)r * u * B * Hu;
-  cudaError_t e;
+// Attention of one or two problems on the kernel for `dt`: bf16 runs both
+// in one tcgen05 launch, fp32 (FP32 pipes) one launch per problem.
+int run_attention(const AttnArgs* a, int n, usp_dtype dt, int64_t D, cudaStream_t s) {
+  for (int i = 0; i < n; ++i)
+    if (a[i].units > 65535) return USP_ERR_UNSUPPORTED;
+  cudaError_t e = cudaSuccess;
   if (dt == USP_F32) {
-    e = launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)out, lse, Nr, Nr, (int)D,
-                        scale, sched, step_heads, s);
+    for (int i = 0; i < n && e == cudaSuccess; ++i) e = launch_attn_f32(a[i], (int)D, s);
   } else {
     Guard g;
     int st = guard(&g);
     if (st != USP_OK) return st;
-    TcAttnArgs a{};
-    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
-    a.Nq = Nr; a.Nk = Nr;
-    a.sched = sched;
-    a.out_step_stride_heads = step_heads;
-    a.fused = false;
-    a.scale = scale;
-    e = launch_attn_tc_fwd(a, g, s);
+    e = launch_attn_tc_fwd(a, n, g, s);
   }
   return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+int run_attention(const AttnArgs& a, usp_dtype dt, int64_t D, cudaStream_t s) {
+  return run_attention(&a, 1, dt, D, s);
+}
+
+// Plain-operand attention arguments: q [q_heads][Nq][D] against k, v [kv_heads][Nk][D].
+AttnArgs plain_args(const void* q, const void* k, const void* v, void* out, float* lse, int64_t Nq,
+                    int64_t q_heads, int64_t Nk, int64_t kv_heads, float scale) {
+  AttnArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+  a.Nq = Nq; a.Nk = Nk;
+  a.q_heads = q_heads; a.kv_heads = kv_heads;
+  a.map.mode = kUnitPlain;
+  a.units = q_heads;
+  a.scale = scale;
+  return a;
+}
+
+// Stack-operand arguments of the fused forward: every (b, h) head attends
+// over all sp shards of its keys (and over the optional text keys).
+AttnArgs stack_args(const void* q, const void* k, const void* v, void* out, float* lse, int64_t BH, int64_t sp,
+                    int64_t Ns, float scale) {
+  AttnArgs a{};
+  a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
+  a.q_stack = a.kv_stack = a.out_stack = true;
+  a.BH = BH; a.sp = sp; a.Ns = Ns;
+  a.map.mode = kUnitPlain;
+  a.units = BH;
+  a.scale = scale;
+  return a;
+}
+
+// Per-(rank, ring step) chunk attention over the head-sharded stacks; ring
+// step t writes output plane t (plane = r*B*H heads of Nr rows).
+AttnArgs ring_args(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B, int64_t Hu,
+                   int64_t Nr, int u, int r, float scale) {
+  const int64_t plane = (int64_t)r * u * B * Hu;
+  AttnArgs a = plain_args(q, k, v, out, lse, Nr, plane, Nr, plane, scale);
+  a.map.mode = kUnitRing;
+  a.map.sched = RingSchedule{u, r, r, (int)(B * Hu)};
+  a.map.out_step_stride = plane;
+  a.units = (int64_t)r * plane;
+  return a;
+}
+int chunk_attention(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B,
+                    int64_t Hu, int64_t Nr, int64_t D, int u, int r, float scale, usp_dtype dt,
+                    cudaStream_t s) {
+  return run_attention(ring_args(q, k, v, out, lse, B, Hu, Nr, u, r, scale), dt, D, s);
 }
 
 }  // namespace
@@ -208,26 +274,8 @@ int usp_attn_chunk_fwd(const void* q, const void* k, const void* v, void* out, f
   if (dtype == USP_BF16 && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16)))
     return USP_ERR_INVALID_ARG;
   if (!aligned(lse, 4)) return USP_ERR_INVALID_ARG;
-  cudaStream_t s = (cudaStream_t)stream;
-  RingSchedule sched{1, 1, 1, (int)(B * H)};
-  cudaError_t e;
-  if (dtype == USP_F32) {
-    e = launch_attn_f32((const float*)q, (const float*)k, (const float*)v, (float*)out, lse, Nq, Nk, (int)D,
-                        scale, sched, 0, s);
-  } else {
-    Guard g;
-    st = guard(&g);
-    if (st != USP_OK) return st;
-    TcAttnArgs a{};
-    a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
-    a.Nq = Nq; a.Nk = Nk;
-    a.sched = sched;
-    a.out_step_stride_heads = 0;
-    a.fused = false;
-    a.scale = scale;
-    e = launch_attn_tc_fwd(a, g, s);
-  }
-  return e == cudaSuccess ? USP_OK : cuda_fail(e);
+  return run_attention(plain_args(q, k, v, out, lse, Nq, B * H, Nk, B * H, scale), dtype, D,
+                       (cudaStream_t)stream);
 }
 
 int usp_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse, int64_t B, int64_t H,
@@ -267,25 +315,10 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
   cudaStream_t s = (cudaStream_t)stream;
 
   if (mode == USP_FUSED) {
-    if (B * H > 65535) return USP_ERR_UNSUPPORTED;
-    cudaError_t e;
-    if (dtype == USP_F32) {
-      e = launch_attn_f32_fused((const float*)q, (const float*)k, (const float*)v, (float*)out, lse, B * H, sp,
-                                Ns, (int)D, scale, s);
-    } else {
-      Guard g;
-      st = guard(&g);
-      if (st != USP_OK) return st;
-      TcAttnArgs a{};
-      a.q = q; a.k = k; a.v = v; a.out = out; a.lse = lse;
-      a.fused = true;
-      a.BH = B * H; a.sp = sp; a.Ns = Ns;
-      a.scale = scale;
-      phase_begin(s);
-      e = launch_attn_tc_fwd(a, g, s);
-      phase_mark(s);
-    }
-    return e == cudaSuccess ? USP_OK : cuda_fail(e);
+    if (dtype == USP_BF16) phase_begin(s);
+    st = run_attention(stack_args(q, k, v, out, lse, B * H, sp, Ns, scale), dtype, D, s);
+    if (st == USP_OK && dtype == USP_BF16) phase_mark(s);
+    return st;
   }
 
   // materialised
@@ -319,6 +352,166 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
   st = relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s);
   phase_mark(s);
   return st;
+}
+
+size_t usp_attention_joint_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses,
+                                           int ring, usp_dtype dtype, usp_mode mode, int with_text_queries) {
+  if (Nt < 0) return 0;
+  if (Nt == 0) return usp_attention_workspace_bytes(B, H, N, D, ulysses, ring, dtype, mode, 0);
+  if (check_dims(B, H, N, D, ulysses, ring) != USP_OK || check_kernel(dtype, D) != USP_OK) return 0;
+  if (mode == USP_FUSED) return 0;
+  return joint_layout(B, H, N, Nt, D, ring, dtype, with_text_queries != 0).total;
+}
+
+int usp_attention_fwd_joint(const void* q, const void* k, const void* v, const void* q_txt, const void* k_txt,
+                            const void* v_txt, void* out, float* lse, void* out_txt, float* lse_txt, int64_t B,
+                            int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses, int ring, float scale,
+                            usp_dtype dtype, usp_mode mode, void* workspace, size_t workspace_bytes,
+                            usp_stream_t stream) {
+  if (Nt < 0) return USP_ERR_INVALID_ARG;
+  if (Nt == 0)
+    return usp_attention_fwd(q, k, v, out, lse, B, H, N, D, ulysses, ring, scale, dtype, mode, workspace,
+                             workspace_bytes, stream);
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  if (mode != USP_MATERIALISED && mode != USP_FUSED) return USP_ERR_INVALID_ARG;
+  st = check_kernel(dtype, D);
+  if (st != USP_OK) return st;
+  if (B * H == 0) return USP_OK;
+  const bool tq = q_txt != nullptr;
+  if (!k_txt || !v_txt || (N > 0 && (!q || !k || !v || !out || !lse)) || (tq && (!out_txt || !lse_txt)))
+    return USP_ERR_INVALID_ARG;
+  if (dtype == USP_BF16) {
+    const void* ptrs[8] = {q, k, v, out, q_txt, k_txt, v_txt, out_txt};
+    for (const void* p : ptrs)
+      if (p && !aligned(p, 16)) return USP_ERR_INVALID_ARG;
+  }
+  if (!aligned(lse, 4) || !aligned(lse_txt, 4)) return USP_ERR_INVALID_ARG;
+  const int u = ulysses, r = ring;
+  const int64_t sp = (int64_t)u * r, Ns = N / sp, Nr = N / r, Hu = H / u, BH = B * H;
+  const int64_t plane = (int64_t)r * BH;  // heads of one partial plane of the head-sharded stack
+  cudaStream_t s = (cudaStream_t)stream;
+  const bool prof = dtype == USP_BF16;
+
+  if (mode == USP_FUSED) {
+    // image queries over the image stack then the text; text queries the same
+    AttnArgs a[2];
+    int n = 0;
+    if (N > 0) {
+      a[n] = stack_args(q, k, v, out, lse, BH, sp, Ns, scale);
+      a[n].k2 = k_txt; a[n].v2 = v_txt; a[n].Nk2 = Nt; a[n].kv2_heads = BH;
+      ++n;
+    }
+    if (tq) {
+      AttnArgs& t = a[n++];
+      t = stack_args(q_txt, k, v, out_txt, lse_txt, BH, sp, Ns, scale);
+      t.q_stack = t.out_stack = false;
+      t.Nq = Nt; t.q_heads = BH;
+      t.k2 = k_txt; t.v2 = v_txt; t.Nk2 = Nt; t.kv2_heads = BH;
+      if (N == 0) {  // text keys only
+        t.k = k_txt; t.v = v_txt; t.kv_stack = false; t.Nk = Nt; t.kv_heads = BH;
+        t.k2 = t.v2 = nullptr; t.Nk2 = 0;
+      }
+    }
+    if (n == 0) return USP_OK;
+    if (prof) phase_begin(s);
+    if ((st = run_attention(a, n, dtype, D, s)) != USP_OK) return st;
+    if (prof) phase_mark(s);
+    return USP_OK;
+  }
+
+  // materialised
+  const JointWorkspace w = joint_layout(B, H, N, Nt, D, r, dtype, tq);
+  if (!workspace || workspace_bytes < w.total) return USP_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return USP_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  const int elt = (int)elt_size(dtype);
+  UnitMap joint_map{};
+  joint_map.sched = RingSchedule{u, r, r, (int)(B * Hu)};
+  joint_map.B = B; joint_map.H = H; joint_map.Hu = Hu;
+  float* tl = (float*)(ws + w.tparts_l);
+  // Partial attention launches.  Each pairs the image queries with the text
+  // queries that read the same K/V: (A) the head-sharded image chunks --
+  // ring steps of the image queries (planes 0..r-1) and the text queries of
+  // head group j against chunk c of that group (text planes 0..r-1); (B) the
+  // text K/V -- image queries of rank (g, j) against the text of head group
+  // j (plane r) and the text queries against the text (last text plane).
+  AttnArgs img_img, txt_img, img_txt, txt_txt;
+  if (N > 0) {
+    img_img = ring_args(ws + w.xq, ws + w.xk, ws + w.xv, ws + w.parts_o, (float*)(ws + w.parts_l), B, Hu, Nr, u, r,
+                        scale);
+    txt_img = plain_args(q_txt, ws + w.xk, ws + w.xv, ws + w.tparts_o, tl, Nt, BH, Nr, plane, scale);
+    txt_img.map = joint_map;
+    txt_img.map.mode = kUnitTxtImg;
+    txt_img.map.out_step_stride = BH;
+    txt_img.units = plane;
+    img_txt = plain_args(ws + w.xq, k_txt, v_txt, ws + w.parts_o, (float*)(ws + w.parts_l), Nr, plane, Nt, BH,
+                         scale);
+    img_txt.map = joint_map;
+    img_txt.map.mode = kUnitImgTxt;
+    img_txt.map.out_base = (int64_t)r * plane;
+    img_txt.units = plane;
+  }
+  const int R_txt = N > 0 ? r + 1 : 1;
+  txt_txt = plain_args(q_txt, k_txt, v_txt, ws + w.tparts_o, tl, Nt, BH, Nt, BH, scale);
+  txt_txt.map.out_base = (int64_t)(R_txt - 1) * BH;
+
+  if (prof) phase_begin(s);
+  if (N > 0) {
+    const void* srcs[3] = {q, k, v};
+    void* dsts[3] = {ws + w.xq, ws + w.xk, ws + w.xv};
+    cudaError_t e = launch_relayout_n(srcs, dsts, 3, B, H, Ns, D, u, r, elt, true, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (prof) phase_mark(s);
+    AttnArgs A[2] = {img_img, txt_img};
+    if ((st = run_attention(A, tq ? 2 : 1, dtype, D, s)) != USP_OK) return st;
+  }
+  {
+    AttnArgs Bt[2];
+    int n = 0;
+    if (N > 0) Bt[n++] = img_txt;
+    if (tq) Bt[n++] = txt_txt;
+    if (n > 0 && (st = run_attention(Bt, n, dtype, D, s)) != USP_OK) return st;
+  }
+  if (prof) phase_mark(s);
+  if (N > 0) {
+    cudaError_t e = launch_lse_merge(ws + w.parts_o, (const float*)(ws + w.parts_l), r + 1, ws + w.xo,
+                                     (float*)(ws + w.xl), BH * N, D, (int)dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (prof) phase_mark(s);
+    if ((st = relayout(ws + w.xo, out, B, H, N, D, u, r, elt, false, s)) != USP_OK) return st;
+    if ((st = relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s)) != USP_OK) return st;
+    if (prof) phase_mark(s);
+  }
+  if (tq) {
+    cudaError_t e = launch_lse_merge(ws + w.tparts_o, tl, R_txt, out_txt, lse_txt, BH * Nt, D, (int)dtype, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (prof) phase_mark(s);
+  }
+  return USP_OK;
+}
+
+int usp_cross_attention_fwd(const void* q, const void* k_txt, const void* v_txt, void* out, float* lse, int64_t B,
+                            int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses, int ring, float scale,
+                            usp_dtype dtype, usp_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || D < 1 || ulysses < 1 || ring < 1) return USP_ERR_INVALID_ARG;
+  if (Nt < 1) return USP_ERR_INVALID_ARG;  // softmax over an empty key set is undefined
+  if (N % ((int64_t)ulysses * ring) != 0) return USP_ERR_DIVISIBILITY;
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  int st = check_kernel(dtype, D);
+  if (st != USP_OK) return st;
+  if (B * H * N == 0) return USP_OK;
+  if (!q || !k_txt || !v_txt || !out || !lse) return USP_ERR_INVALID_ARG;
+  if (dtype == USP_BF16 && !(aligned(q, 16) && aligned(k_txt, 16) && aligned(v_txt, 16) && aligned(out, 16)))
+    return USP_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return USP_ERR_INVALID_ARG;
+  const int64_t sp = (int64_t)ulysses * ring, BH = B * H;
+  AttnArgs a = stack_args(q, k_txt, v_txt, out, lse, BH, sp, N / sp, scale);
+  a.kv_stack = false;
+  a.Nk = Nt;
+  a.kv_heads = BH;
+  return run_attention(a, dtype, D, (cudaStream_t)stream);
 }
 
 int usp_attention_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,

@@ -25,8 +25,7 @@ struct Guard {
 
 // Problem description for the attention kernels.  A "unit" is one
 // (query head, KV head, output head) triple; the ring schedule maps
-// unit -> heads for the materialised USP launch, the plain chunk call uses
-// the identity.
+// unit -> heads for the materialised USP launch.
 struct RingSchedule {
   int ulysses;   // u  (1 for a plain chunk call)
   int ring;      // r  (1 for a plain chunk call)
@@ -47,30 +46,89 @@ cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int co
 cudaError_t launch_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
                              int64_t rows, int64_t D, int dtype, cudaStream_t stream);
 
-// fp32 attention on the FP32 pipes.  q: [units_q][Nq][D]; k,v: [units_kv][Nk][D].
-cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* out, float* lse,
-                            int64_t Nq, int64_t Nk, int D, float scale, RingSchedule sched,
-                            int64_t out_step_stride_heads, cudaStream_t stream);
-
-// fp32 fused USP forward over token-sharded stacks.
-cudaError_t launch_attn_f32_fused(const float* q, const float* k, const float* v, float* out,
-                                  float* lse, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
-                                  cudaStream_t stream);
-
-// bf16 tcgen05 attention forward (D = 128).
-struct TcAttnArgs {
-  const void* q; const void* k; const void* v;
-  void* out; float* lse;
-  // plain / materialised addressing: heads are contiguous [rows][D] blocks
-  int64_t Nq, Nk;
+// Unit -> heads mappings of the attention kernels.  Head-sharded stack head
+// ((g*u + j)*B + b)*Hu + h' holds rank (g, j)'s slice of plain head
+// b*H + j*Hu + h'.
+enum UnitMode : int {
+  kUnitPlain = 0,   // q head = kv head = unit, out head = out_base + unit
+  kUnitRing = 1,    // materialised ring step t: KV chunk (g - t) mod ring, out plane t
+  kUnitImgTxt = 2,  // unit = stack head: image queries against the text head of their group
+  kUnitTxtImg = 3,  // unit = (c, j, b, h'): text queries of head group j against ring chunk c
+};
+struct UnitMap {
+  int mode;
   RingSchedule sched;
-  int64_t out_step_stride_heads;   // heads between consecutive ring steps in out/lse
-  // fused addressing: token-sharded stack [sp][BH][Ns][D]
-  bool fused;
-  int64_t BH, sp, Ns;
+  int64_t out_step_stride;  // heads between ring steps (output planes)
+  int64_t out_base;         // head offset of the launch's first output head
+  int64_t B, H, Hu;
+};
+struct UnitHeads {
+  int64_t qh, kvh, kvh2, oh;  // kvh2: head of the second KV source
+};
+// Units, heads and ring indices all fit 32 bits (launch grids bound the
+// unit count), so the index arithmetic divides in 32 bits; only the output
+// head offset is formed in 64 bits.
+__device__ __forceinline__ UnitHeads map_unit(const UnitMap& m, int64_t unit64) {
+  UnitHeads r;
+  const int unit = (int)unit64;
+  r.kvh2 = unit;
+  if (m.mode == kUnitPlain) {
+    r.qh = r.kvh = unit;
+    r.oh = m.out_base + unit;
+    return r;
+  }
+  const RingSchedule& s = m.sched;
+  if (m.mode == kUnitRing) {
+    const int per_step = s.ring * s.ulysses * s.heads_per_rank;
+    const int t = unit / per_step;
+    const int qh = unit - t * per_step;
+    const int group = s.heads_per_rank * s.ulysses;  // heads of one ring rank
+    const int g = qh / group;
+    const int c = ((g - t) % s.ring + s.ring) % s.ring;  // KV chunk at ring step t
+    r.qh = qh;
+    r.kvh = qh + (c - g) * group;
+    r.oh = m.out_base + (int64_t)t * m.out_step_stride + qh;
+    return r;
+  }
+  const int Hu = (int)m.Hu, B = (int)m.B;
+  const int hp = unit % Hu, b = (unit / Hu) % B, j = (unit / (Hu * B)) % s.ulysses;
+  const int th = b * (int)m.H + j * Hu + hp;  // plain (text) head of the same (j, b, h')
+  if (m.mode == kUnitImgTxt) {
+    r.qh = unit;
+    r.kvh = th;
+    r.oh = m.out_base + unit;
+    return r;
+  }
+  const int c = unit / (Hu * B * s.ulysses);
+  r.qh = th;
+  r.kvh = ((c * s.ulysses + j) * B + b) * Hu + hp;
+  r.oh = m.out_base + (int64_t)c * m.out_step_stride + th;
+  return r;
+}
+
+// Operands of one attention launch.  A "stack" operand is the token-sharded
+// stack [sp][BH][Ns][D] read as sp*Ns rows per head; a plain operand is
+// [heads][rows][D].  The optional second KV source (plain) follows the first
+// source's keys in the softmax, e.g. the text tokens of joint attention.
+struct AttnArgs {
+  const void* q; const void* k; const void* v;
+  const void* k2; const void* v2;
+  void* out; float* lse;
+  bool q_stack, kv_stack, out_stack;
+  int64_t Nq, Nk, Nk2;                 // rows per head of the plain operands
+  int64_t q_heads, kv_heads, kv2_heads;  // heads of the plain operands
+  int64_t BH, sp, Ns;                  // stack geometry
+  UnitMap map;
+  int64_t units;
   float scale;
 };
-cudaError_t launch_attn_tc_fwd(const TcAttnArgs& a, const Guard& g, cudaStream_t stream);
+
+// fp32 attention on the FP32 pipes (any D <= 128).
+cudaError_t launch_attn_f32(const AttnArgs& a, int D, cudaStream_t stream);
+
+// bf16 tcgen05 attention forward (D = 128): one launch serving one or two
+// problems (same stack geometry and scale).
+cudaError_t launch_attn_tc_fwd(const AttnArgs* sides, int nsides, const Guard& g, cudaStream_t stream);
 
 // bf16 tcgen05 backward over token-sharded stacks (D = 128): prep (Delta,
 // lse*log2e into workspace), dK/dV kernel, dQ kernel.

@@ -50,6 +50,7 @@ class Workload:
     seed: int
     row_seed: int
     description: str
+    Nt: int = 0         # replicated text tokens of joint attention (0: image only)
 
     @property
     def sp(self) -> int:
@@ -96,6 +97,12 @@ class Workload:
         """Algorithmic forward FLOP of non-causal attention: 4*B*H*N^2*D."""
         return 4.0 * self.B * self.H * self.N * self.N * self.D
 
+    def joint_flop(self, text_queries: bool = True) -> float:
+        """Algorithmic FLOP of joint attention: every image (and text) query
+        against all N + Nt keys, 4 FLOP per query-key-dim."""
+        nq = self.N + (self.Nt if text_queries else 0)
+        return 4.0 * self.B * self.H * nq * (self.N + self.Nt) * self.D
+
     @property
     def bwd_flop(self) -> float:
         """Algorithmic backward FLOP: 10*B*H*N^2*D (five N x N x D GEMMs)."""
@@ -113,15 +120,24 @@ WORKLOADS = {
                          "bf16 B1 H40 N32768 D128 ulysses8 x ring4, fwd+bwd (Wan shapes)"),
     "wan720p": Workload("wan720p", "bf16", 1, 40, 75600, 128, 8, 2, False, 1004, 2004,
                         "bf16 B1 H40 N75600 D128 ulysses8 x ring2 (Wan 720p 81 frames)"),
+    # Joint text + image attention: the handbook's per-layer communication
+    # table counts FLUX 1024^2 as 4608 tokens and Wan 720p 81 frames as 76112,
+    # i.e. the image tokens plus 512 text tokens, which the vllm-omni guide
+    # ("How to parallelize a new model") keeps replicated on every SP rank.
+    "qwen1024_joint": Workload("qwen1024_joint", "bf16", 1, 24, 4096, 128, 2, 2, False, 1005, 2005,
+                               "bf16 B1 H24 N4096+512 text D128 ulysses2 x ring2 (joint, 4608 tokens)", 512),
+    "wan720p_joint": Workload("wan720p_joint", "bf16", 1, 40, 75600, 128, 8, 2, False, 1006, 2006,
+                              "bf16 B1 H40 N75600+512 text D128 ulysses8 x ring2 (joint, 76112 tokens)", 512),
 }
 
 ORDER = ["demo", "qwen1024", "qwen2048", "wan_s32k", "wan720p"]
+JOINT = ["qwen1024_joint", "wan720p_joint"]
 
 
-def custom(name, dtype, B, H, N, D, ulysses, ring, seed=7, backward=False) -> Workload:
+def custom(name, dtype, B, H, N, D, ulysses, ring, seed=7, backward=False, Nt=0) -> Workload:
     """A workload of arbitrary shape (used by tests for ragged and edge cases)."""
     return Workload(name, dtype, B, H, N, D, ulysses, ring, backward, seed, seed + 1000,
-                    f"{dtype} B{B} H{H} N{N} D{D} u{ulysses} r{ring}")
+                    f"{dtype} B{B} H{H} N{N} D{D} u{ulysses} r{ring}" + (f" Nt{Nt}" if Nt else ""), Nt)
 
 
 def to_token_stack(x: torch.Tensor, ulysses: int, ring: int) -> torch.Tensor:
@@ -200,3 +216,19 @@ def sample_rows(w: Workload, count: int = 4096) -> torch.Tensor:
         rows.add(int(perm[i]))
         i += 1
     return torch.tensor(sorted(rows), dtype=torch.int64)
+
+
+def make_text_inputs(w: Workload):
+    """Draw the replicated text tensors q_txt, k_txt, v_txt [B, H, Nt, D].
+
+    iid N(0,1) from a CPU generator seeded with ``w.seed + 7919`` (drawn in
+    fp32 in the order q_txt, k_txt, v_txt, then cast), independent of the
+    image draws of :func:`make_inputs`.
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 7919)
+    out = {}
+    for n in ("q_txt", "k_txt", "v_txt"):
+        x = torch.randn(w.B, w.H, w.Nt, w.D, generator=g, dtype=torch.float32)
+        out[n] = x.to(w.torch_dtype)
+    return out

@@ -156,6 +156,53 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
                       int64_t D, int ulysses, int ring, float scale, usp_dtype dtype, void* workspace,
                       size_t workspace_bytes, usp_stream_t stream);
 
+/* Bytes of workspace usp_attention_fwd_joint needs (0 for USP_FUSED);
+ * with_text_queries = 1 when q_txt will be given.  Returns 0 as well for
+ * arguments the call itself would reject. */
+size_t usp_attention_joint_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses,
+                                           int ring, usp_dtype dtype, usp_mode mode, int with_text_queries);
+
+/* Joint text + image USP attention forward ([VO] "How to parallelize a new
+ * model": a dual-stream model attends over the concatenated text and image
+ * sequences; image tokens are chunked across the SP ranks, text embeddings
+ * stay replicated on every rank).  Image tensors q, k, v, out, lse are the
+ * token-sharded stacks of usp_attention_fwd; text tensors k_txt, v_txt (and
+ * q_txt, out_txt) are plain [B, H, Nt, D] in `dtype`, lse_txt [B, H, Nt] fp32,
+ * the same on every virtual rank.  The result equals unsharded attention of
+ * every query over the Nt text + N image keys of its head.
+ *   USP_MATERIALISED: tok2head(q,k,v) -> per rank (g, j) the ring chunk
+ *     partials (as usp_attention_fwd) plus one partial against the text K/V
+ *     of head group j -> merge of ring + 1 partials -> head2tok.  Text
+ *     queries of head group j: one partial per ring chunk c of that group
+ *     (the same on every ring rank, computed once) plus one against the
+ *     text K/V -> merge into out_txt, lse_txt.
+ *   USP_FUSED: one kernel launch reads the stacks and the text in place
+ *     (image and text queries share it); the text K/V are the last KV tiles
+ *     of the online softmax.
+ * q_txt may be NULL (no text queries: out_txt, lse_txt are then ignored).
+ * Nt = 0 is usp_attention_fwd.
+ * Errors: INVALID_ARG (null, negative Nt, misaligned, non-finite scale),
+ * DIVISIBILITY, UNSUPPORTED, WORKSPACE, CUDA. */
+int usp_attention_fwd_joint(const void* q, const void* k, const void* v, const void* q_txt, const void* k_txt,
+                            const void* v_txt, void* out, float* lse, void* out_txt, float* lse_txt, int64_t B,
+                            int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses, int ring, float scale,
+                            usp_dtype dtype, usp_mode mode, void* workspace, size_t workspace_bytes,
+                            usp_stream_t stream);
+
+/* Cross-attention under sequence parallelism ([PR]: replicated K/V make
+ * local attention exact and it follows the stock path; [VO] "How to
+ * parallelize a new model": text embeddings stay replicated on every SP
+ * rank).  q, out: token-sharded image stacks [ring, ulysses, B, H, Ns, D];
+ * lse: [ring, ulysses, B, H, Ns] fp32; k_txt, v_txt: plain [B, H, Nt, D],
+ * the same on every virtual rank.  Every rank attends its own query tokens to
+ * the complete text K/V: one kernel launch, no re-layout, no merge.  The
+ * result equals unsharded attention of the image queries against the text.
+ * Errors: INVALID_ARG (null, Nt < 1, misaligned, non-finite scale),
+ * DIVISIBILITY (N % (ulysses*ring)), UNSUPPORTED, CUDA. */
+int usp_cross_attention_fwd(const void* q, const void* k_txt, const void* v_txt, void* out, float* lse,
+                            int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses, int ring,
+                            float scale, usp_dtype dtype, usp_stream_t stream);
+
 /* The materialised forward (same arguments, layouts, result and errors as
  * usp_attention_fwd with mode USP_MATERIALISED) for callers that cannot
  * allocate device memory: code running under a framework whose caching
@@ -182,6 +229,10 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *   fused forward:        [attention]
  *   materialised forward: [tok2head q,k,v] [chunk attention] [merge] [head2tok x2]
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
+ *   joint fused:          [attention: image and text queries, one launch]
+ *   joint materialised:   [tok2head q,k,v] [partials against the image chunks
+ *                         and against the text] [merge] [head2tok x2]
+ *                         [text-query merge]
  * (the fp32 paths record nothing).  The events
  * are created by the library on first enable.  Returns USP_OK or USP_ERR_CUDA. */
 int usp_profile_phases(int enable);

@@ -95,6 +95,44 @@ def test_attention_validation_and_workspace(L):
     assert f(None, None, None, None, None, 1, 8, 0, 32, 4, 1, 0.1, 0, 1, None, 0, None) == 0  # empty
 
 
+def test_joint_validation_and_workspace(L):
+    f = L.usp_attention_fwd_joint
+    img = (FAKE, FAKE, FAKE)
+    txt = (FAKE, FAKE, FAKE)
+    outs = (FAKE, FAKE, FAKE, FAKE)
+    base = (1, 24, 4096, 512, 128, 2, 2, 0.1, 1)
+    assert f(*img, *txt, *outs, 1, 24, 4096, -1, 128, 2, 2, 0.1, 1, 0, None, 0, None) == 1   # negative Nt
+    assert f(*img, *txt, *outs, 1, 24, 4098, 512, 128, 2, 2, 0.1, 1, 0, None, 0, None) == 2  # N % sp
+    assert f(*img, *txt, *outs, 1, 24, 4096, 512, 64, 2, 2, 0.1, 1, 0, None, 0, None) == 3   # bf16 D != 128
+    assert f(*img, FAKE, None, FAKE, *outs, *base, 0, None, 0, None) == 1                      # k_txt missing
+    assert f(*img, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, *base, 0, None, 0, None) == 1     # out_txt missing
+    assert f(*img, *txt, *outs, *base, 0, None, 0, None) == 4                                   # no workspace
+    assert f(*img, *txt, *outs, *base, 7, None, 0, None) == 1                                   # bad mode
+    assert f(*img, FAKE + 2, FAKE, FAKE, *outs, *base, 1, None, 0, None) == 1                  # misaligned q_txt
+    t, lb = 24 * 4096 * 128 * 2, 24 * 4096 * 4
+    tt, tlb = 24 * 512 * 128 * 2, 24 * 512 * 4
+    ws = L.usp_attention_joint_workspace_bytes(1, 24, 4096, 512, 128, 2, 2, 1, 0, 1)
+    assert ws == 3 * t + 3 * t + 3 * lb + t + lb + 3 * tt + 3 * tlb
+    assert L.usp_attention_joint_workspace_bytes(1, 24, 4096, 512, 128, 2, 2, 1, 0, 0) == ws - 3 * tt - 3 * tlb
+    assert f(*img, *txt, *outs, *base, 0, FAKE, ws - 1, None) == 4
+    assert L.usp_attention_joint_workspace_bytes(1, 24, 4096, 512, 128, 2, 2, 1, 1, 1) == 0   # fused: none
+    assert L.usp_attention_joint_workspace_bytes(1, 24, 4096, 0, 128, 2, 2, 1, 0, 1) == \
+        L.usp_attention_workspace_bytes(1, 24, 4096, 128, 2, 2, 1, 0, 0)                        # Nt = 0
+    assert f(None, None, None, None, FAKE, FAKE, None, None, None, None, 0, 24, 4096, 512, 128, 2, 2, 0.1, 1, 1,
+             None, 0, None) == 0                                                                # empty batch
+
+
+def test_cross_attention_validation(L):
+    f = L.usp_cross_attention_fwd
+    a = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert f(*a, 1, 40, 75600, 0, 128, 8, 2, 0.1, 1, None) == 1        # no text keys
+    assert f(*a, 1, 40, 75601, 512, 128, 8, 2, 0.1, 1, None) == 2     # N % sp
+    assert f(*a, 1, 40, 75600, 512, 64, 8, 2, 0.1, 1, None) == 3      # bf16 D != 128
+    assert f(*a, 1, 40, 75600, 512, 128, 8, 2, float("nan"), 1, None) == 1
+    assert f(FAKE + 8, *a[1:], 1, 40, 75600, 512, 128, 8, 2, 0.1, 1, None) == 1   # misaligned q
+    assert f(None, None, None, None, None, 1, 40, 0, 512, 128, 8, 2, 0.1, 1, None) == 0  # empty
+
+
 def test_product_path_does_not_import_oracle():
     import subprocess
     import sys
