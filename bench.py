@@ -500,13 +500,19 @@ def our_arm(args, w, ws, rank, local):
     if step.joint:
         kernels = {"attn_tc_fwd_kernel": (fused_s, fwd_flop,
                                           "fused joint forward (image and text queries, one launch per call)")}
+    overlapped = {}
     if bwd_phases and len(bwd_phases[0]) == 3:
         dkdv_s = statistics.mean(p[1] for p in bwd_phases)
         dq_s = statistics.mean(p[2] for p in bwd_phases)
         # algorithmic work: dK/dV kernel = 4 of the 5 backward GEMMs (S, dP, dV, dK);
-        # dQ kernel = the dQ GEMM (its recomputation of S and dP is not counted)
+        # dQ kernel = the dQ GEMM (its recomputation of S and dP is not counted).
+        # The dQ kernel runs concurrently with dK/dV (launched second, its CTAs fill dK/dV's last
+        # wave), so its event time (from the end of the prep to its own end) includes the time its
+        # CTAs waited for SMs: it is reported, but only dK/dV (launched first, alone on the GPU until
+        # its tail) and the fused forward are roofline candidates.  Dominance by serialised device
+        # time: profiles/launches_qwen1024_step.md.
         kernels["usp_bwd_dkdv_kernel"] = (dkdv_s, 0.8 * w.bwd_flop, "backward dK/dV (S^T, dP^T, dV, dK GEMMs)")
-        kernels["usp_bwd_dq_kernel"] = (dq_s, 0.2 * w.bwd_flop, "backward dQ (dQ GEMM; S, dP recompute uncounted)")
+        overlapped["usp_bwd_dq_kernel_overlapped_ms"] = dq_s * 1e3
     dom = max(kernels, key=lambda k: kernels[k][0])
     t_dom, f_dom, desc = kernels[dom]
     ach = f_dom / t_dom / 1e12
@@ -542,6 +548,7 @@ def our_arm(args, w, ws, rank, local):
                      "bwd_tflops": w.bwd_flop / statistics.mean(bwd) / 1e12} if step.backward else {}),
                  **({k + "_ms": v[0] * 1e3 for k, v in kernels.items()}),
                  **({k + "_tflops": v[1] / v[0] / 1e12 for k, v in kernels.items()}),
+                 **overlapped,
                  **{k + "_GBps": v["GB/s"] for k, v in rows.items()},
                  **{k + "_tflops": v["TFLOP/s"] for k, v in rows.items() if "TFLOP/s" in v},
                  **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items()}},

@@ -683,7 +683,7 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
       (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, a.delta, a.l2, rows, a.Ns, Ns_pad);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  phase_mark(stream);
+  const int prep_mark = phase_mark(stream);
   CUtensorMap mq, mk, mv, mdo, ml2, mdl;
   if (!map_stack_bf16(&mq, a.q, a.Ns, a.BH, a.sp) || !map_stack_bf16(&mk, a.k, a.Ns, a.BH, a.sp) ||
       !map_stack_bf16(&mv, a.v, a.Ns, a.BH, a.sp) || !map_stack_bf16(&mdo, a.dout, a.Ns, a.BH, a.sp) ||
@@ -701,18 +701,27 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   p.scale_log2 = a.scale * LOG2E;
   p.guard = g;
   dim3 grid((unsigned)p.tiles, (unsigned)a.BH, 1);
+  // The two kernels are independent (each writes its own gradients): dQ runs
+  // on the device's side stream, so its CTAs fill the dK/dV kernel's last,
+  // partial wave instead of waiting behind it.
+  cudaStream_t side = nullptr;
+  e = side_begin(stream, &side);
+  if (e != cudaSuccess) return e;
+  BwdParams pq = p;
   p.dst0 = a.dk;
   p.dst1 = a.dv;
   usp_bwd_dkdv_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mdo, ml2, mdl, p);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  phase_mark(stream);
-  p.dst0 = a.dq;
-  p.dst1 = nullptr;
-  usp_bwd_dq_kernel<<<grid, NUM_THREADS, DQ_SMEM_BYTES, stream>>>(mq, mk, mv, mdo, p);
-  e = cudaGetLastError();
-  phase_mark(stream);
-  return e;
+  phase_mark(stream, prep_mark);
+  pq.dst0 = a.dq;
+  pq.dst1 = nullptr;
+  if (e == cudaSuccess) {
+    usp_bwd_dq_kernel<<<grid, NUM_THREADS, DQ_SMEM_BYTES, side>>>(mq, mk, mv, mdo, pq);
+    e = cudaGetLastError();
+  }
+  phase_mark(side, prep_mark);
+  const cudaError_t j = side_end(stream);  // always join, also after a failed launch
+  return e != cudaSuccess ? e : j;
 }
 
 }  // namespace usp

@@ -33,13 +33,18 @@ struct PhaseState {
   bool created = false;
   int marks = 0;
   cudaEvent_t ev[kMaxPhases + 1];
+  int from[kMaxPhases + 1];  // phase i runs from event from[i] to event i
 };
 thread_local PhaseState t_phase;
 
 }  // namespace
-void phase_mark(cudaStream_t s) {
-  if (!t_phase.enabled || t_phase.marks == 0 || t_phase.marks > kMaxPhases) return;
-  if (cudaEventRecord(t_phase.ev[t_phase.marks], s) == cudaSuccess) ++t_phase.marks;
+int phase_mark(cudaStream_t s, int from) {
+  if (!t_phase.enabled || t_phase.marks == 0 || t_phase.marks > kMaxPhases) return -1;
+  const int i = t_phase.marks;
+  if (cudaEventRecord(t_phase.ev[i], s) != cudaSuccess) return -1;
+  t_phase.from[i] = (from >= 0 && from < i) ? from : i - 1;
+  ++t_phase.marks;
+  return i;
 }
 namespace {
 void phase_begin(cudaStream_t s) {
@@ -86,6 +91,14 @@ int guard(Guard* g) {
   g->ns_limit = kWaitNs;
   return USP_OK;
 }
+
+// Per-device side stream for a kernel that may overlap the caller's stream.
+struct SideSlot {
+  std::mutex mu;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideSlot g_side[kMaxDevices];
 
 size_t elt_size(usp_dtype d) { return d == USP_BF16 ? 2 : 4; }
 bool dtype_ok(usp_dtype d) { return d == USP_F32 || d == USP_BF16; }
@@ -235,6 +248,44 @@ int chunk_attention(const void* q, const void* k, const void* v, void* out, floa
 }
 
 }  // namespace
+
+cudaError_t side_begin(cudaStream_t main, cudaStream_t* side) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideSlot& sl = g_side[dev];
+  sl.mu.lock();
+  if (!sl.stream) {
+    e = cudaStreamCreateWithFlags(&sl.stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.fork, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      sl.mu.unlock();
+      return e;
+    }
+  }
+  e = cudaEventRecord(sl.fork, main);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sl.stream, sl.fork, 0);
+  if (e != cudaSuccess) {
+    sl.mu.unlock();
+    return e;
+  }
+  *side = sl.stream;
+  return cudaSuccess;
+}
+
+cudaError_t side_end(cudaStream_t main) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;  // cannot happen after side_begin succeeded on this thread
+  SideSlot& sl = g_side[dev];
+  e = cudaEventRecord(sl.join, sl.stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(main, sl.join, 0);
+  sl.mu.unlock();
+  return e;
+}
+
 }  // namespace usp
 
 using namespace usp;
@@ -609,10 +660,12 @@ int usp_profile_phases(int enable) {
 int usp_profile_read(float* ms, int max_phases) {
   if (!t_phase.created || t_phase.marks < 2) return 0;
   const int n = t_phase.marks - 1;
-  cudaError_t e = cudaEventSynchronize(t_phase.ev[n]);
-  if (e != cudaSuccess) return -cuda_fail(e);
+  for (int i = 1; i <= n; ++i) {  // phases may end on different streams
+    cudaError_t e = cudaEventSynchronize(t_phase.ev[i]);
+    if (e != cudaSuccess) return -cuda_fail(e);
+  }
   for (int i = 0; i < n && i < max_phases; ++i) {
-    e = cudaEventElapsedTime(&ms[i], t_phase.ev[i], t_phase.ev[i + 1]);
+    cudaError_t e = cudaEventElapsedTime(&ms[i], t_phase.ev[t_phase.from[i + 1]], t_phase.ev[i + 1]);
     if (e != cudaSuccess) return -cuda_fail(e);
   }
   return n < max_phases ? n : max_phases;

@@ -149,8 +149,18 @@ cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, 
                                 float* delta, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
                                 cudaStream_t stream);
 
-// Records the next phase event of the current call (no-op unless phase timing
-// is enabled with usp_profile_phases).
-void phase_mark(cudaStream_t s);
+// Records the next phase event of the current call on stream `s` (no-op
+// unless phase timing is enabled with usp_profile_phases).  The phase runs
+// from event `from` (an earlier mark's return value; -1 = the previous mark)
+// to this one.  Returns this mark's index, or -1.
+int phase_mark(cudaStream_t s, int from = -1);
+
+// Fork / join of the device's side stream: side_begin makes the side stream
+// wait for the work enqueued so far on `main` and hands it out (holding the
+// device's side-stream lock); side_end makes `main` wait for everything
+// enqueued on the side stream and releases the lock.  Every successful
+// side_begin must be followed by side_end on the same thread and device.
+cudaError_t side_begin(cudaStream_t main, cudaStream_t* side);
+cudaError_t side_end(cudaStream_t main);
 
 }  // namespace usp

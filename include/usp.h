@@ -150,6 +150,11 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
  *   dS = P * (dP - Delta), dQ = scale dS K, dK = scale dS^T Q.
  * q, k, v, out, dout, dq, dk, dv: token-sharded stacks in `dtype`; lse: the
  * forward's fp32 LSE.  Needs usp_attention_workspace_bytes(..., 1).
+ * The bf16 path runs its dQ kernel concurrently with the dK/dV kernel on a
+ * library-owned stream of the current device, forked from and joined back to
+ * `stream` with events (so the call stays ordered on `stream` and can be
+ * captured into a CUDA graph); concurrent calls on one device take turns on
+ * that stream.
  * Errors: as usp_attention_fwd. */
 int usp_attention_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
@@ -229,6 +234,8 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *   fused forward:        [attention]
  *   materialised forward: [tok2head q,k,v] [chunk attention] [merge] [head2tok x2]
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
+ *                         (the two kernels run concurrently; both phases
+ *                         are timed from the end of the prep)
  *   joint fused:          [attention: image and text queries, one launch]
  *   joint materialised:   [tok2head q,k,v] [partials against the image chunks
  *                         and against the text] [merge] [head2tok x2]

@@ -108,3 +108,73 @@ def test_bwd_wan_shapes_sampled():
     _check_grad(g_dq, r_dq, "bf16", "wan dq")
     _check_grad(g_dk, r_dk, "bf16", "wan dk")
     _check_grad(g_dv, r_dv, "bf16", "wan dv")
+
+
+def _small_bwd_inputs(seed=21):
+    w = wl.custom("bwdc", "bf16", 1, 4, 1024, 128, 2, 2, seed=seed, backward=True)
+    inp = wl.make_inputs(w)
+    st = {n: wl.to_token_stack(t, 2, 2).cuda() for n, t in inp.items()}
+    return w, st
+
+
+def test_bwd_concurrent_kernels_graph_capture():
+    """The backward's dQ kernel runs on a library-owned side stream, forked and
+    joined with events: captured into a CUDA graph and replayed it must give
+    the eager result bit for bit."""
+    usp = _usp()
+    w, st = _small_bwd_inputs()
+    o, l = usp.attention_fwd(st["q"], st["k"], st["v"], 2, 2, w.scale, mode="fused")
+    ref = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+    torch.cuda.synchronize()
+    ws = torch.empty(usp.workspace_bytes(w.B, w.H, w.N, w.D, 2, 2, torch.bfloat16, backward=True),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):   # warm-up on the capture stream
+        usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        got = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, workspace=ws)
+    for _ in range(2):
+        for t in got:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(got, ref):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert usp.device_status() == 0
+
+
+def test_bwd_two_host_threads():
+    """Two host threads, each on its own stream, share the device's side stream
+    (it is locked per call): every result equals the single-thread one."""
+    import threading
+    usp = _usp()
+    w, st = _small_bwd_inputs(seed=22)
+    o, l = usp.attention_fwd(st["q"], st["k"], st["v"], 2, 2, w.scale, mode="fused")
+    ref = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker():
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(8):
+                    got = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+                    s.synchronize()
+                    for a, b in zip(got, ref):
+                        if not torch.equal(a.view(torch.int16), b.view(torch.int16)):
+                            errors.append("mismatch")
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    ts = [threading.Thread(target=worker) for _ in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+    assert usp.device_status() == 0
