@@ -11,11 +11,14 @@ from .usp_oracle import (  # noqa: F401
     attention_bwd,
     attention_bwd_sampled,
     attention_rows,
+    e4m3_round,
     head2tok,
     lse_merge,
+    quantize_e4m3_heads,
     ring_chunk,
     tok2head,
     usp_cross_attention,
     usp_forward,
+    usp_forward_fp8,
     usp_forward_joint,
 )

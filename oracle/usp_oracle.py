@@ -49,6 +49,17 @@ Readings where the pages are silent or open:
   ring chunk of their Ulysses head group.
 * Cross-attention: each rank's image queries attend to the replicated text
   K/V only; nothing is exchanged.
+* FP8 attention (the handbook's Wan table: "FP8 low precision" as the last
+  latency step; the pages print no scheme): q, k and v are quantised to
+  OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+  infinities, largest finite 448, round to nearest even, saturating) with
+  one scale per (b, h) head over the whole sequence, amax / 448; the
+  attention then runs on the dequantised values.  The quantisation decision
+  is taken in fp32 exactly as a kernel takes it (inv = 448 / amax and
+  x * inv, both IEEE fp32 round to nearest), so codes can be compared bit
+  for bit.  The kernel's rounding of the probabilities P to E4M3 for the
+  P V product depends on its running maximum and is not modelled here; its
+  effect is bounded statistically instead.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 library routines (torch fp64 SDPA and autograd on CPU), closed forms,
@@ -333,4 +344,59 @@ def usp_cross_attention(Tq, k_txt, v_txt, ulysses: int, ring: int, scale: float)
         for j in range(ulysses):
             O[g, j], L[g, j] = attention(Tq[g, j], kt, vt, scale)
     return O, L
+
+
+# ------------------------------------------------------------------ FP8 E4M3
+E4M3_MAX = 448.0
+
+
+def e4m3_round(x):
+    """Round to the nearest OCP E4M3 value, ties to even, saturating at +-448.
+
+    E4M3 has normal values (1 + m/8) * 2**(e - 7) for exponent field e in
+    1..15 (e = 15, m = 7 is NaN, so the largest finite value is 1.75 * 2**8 =
+    448) and subnormals (m/8) * 2**-6.  Every binade above 2**-6 therefore
+    holds 8 values spaced 2**(E - 3), and below it the spacing is 2**-9:
+    the grid spacing at |x| is 2**(max(floor(log2|x|), -6) - 3).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(np.where(a > 0, a, 1.0))      # a = f * 2**e, 0.5 <= f < 1: floor(log2 a) = e - 1
+    E = np.maximum(e - 1, -6)
+    quantum = np.ldexp(1.0, E - 3)
+    y = np.round(a / quantum) * quantum            # np.round: half to even (exact: quantum is a power of 2)
+    y = np.minimum(y, E4M3_MAX)
+    return np.where(a > 0, np.sign(x) * y, 0.0)
+
+
+def quantize_e4m3_heads(T):
+    """Per-head E4M3 quantisation of a token-sharded stack [r, u, B, H, Ns, D].
+
+    One scale per (b, h) over every shard, token and dimension:
+    inv = fp32(448) / fp32(amax), code value = e4m3(fp32(x) * inv) (both fp32
+    operations round to nearest), dequantisation scale = fp32(amax) / fp32(448);
+    amax = 0 gives inv = scale = 1.  Returns (codes as fp64 values on the E4M3
+    grid, scales [B, H] fp64 holding the fp32 values).
+    """
+    T32 = np.asarray(T, dtype=np.float32)
+    amax = np.abs(T32).max(axis=(0, 1, 4, 5))                              # [B, H], exact
+    nz = amax > 0
+    inv = np.where(nz, np.float32(E4M3_MAX) / np.where(nz, amax, np.float32(1)), np.float32(1)).astype(np.float32)
+    scale = np.where(nz, amax / np.float32(E4M3_MAX), np.float32(1)).astype(np.float32)
+    prod = (T32 * inv[None, None, :, :, None, None]).astype(np.float32)   # fp32 multiply, round to nearest
+    return e4m3_round(prod.astype(np.float64)), scale.astype(np.float64)
+
+
+def usp_forward_fp8(Tq, Tk, Tv, ulysses: int, ring: int, scale: float):
+    """FP8 USP forward: q, k, v quantised per head to E4M3, then the USP
+    forward of the dequantised values (equal to unsharded attention of them).
+    Returns (O, LSE, (codes_q, codes_k, codes_v), (scale_q, scale_k, scale_v))."""
+    codes, scales = [], []
+    for T in (Tq, Tk, Tv):
+        c, sc = quantize_e4m3_heads(T)
+        codes.append(c)
+        scales.append(sc)
+    deq = [c * sc[None, None, :, :, None, None] for c, sc in zip(codes, scales)]
+    O, L = usp_forward(*deq, ulysses, ring, scale)
+    return O, L, tuple(codes), tuple(scales)
 

@@ -229,6 +229,92 @@ def test_ring_chunk_schedule_visits_every_chunk_once():
             assert uo.ring_chunk(g, 0, r) == g
 
 
+# ------------------------------------------------------------------ FP8 E4M3
+
+def _e4m3_table():
+    """Every finite E4M3 value, decoded from the bit fields: (value, code)."""
+    vals = []
+    for code in range(256):
+        sgn, e, m = code >> 7, (code >> 3) & 15, code & 7
+        if e == 15 and m == 7:
+            continue                                   # NaN encodings
+        mag = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+        vals.append(((-1) ** sgn * mag, code))
+    return vals
+
+
+def test_e4m3_grid_fixed_points_and_extremes():
+    table = _e4m3_table()
+    v = np.array([t[0] for t in table])
+    np.testing.assert_array_equal(uo.e4m3_round(v), v)
+    assert v.max() == 448.0 and v.min() == -448.0
+    assert np.min(np.abs(v[v != 0])) == 2.0 ** -9
+
+
+def test_e4m3_round_is_nearest_ties_to_even_brute_force():
+    table = [t for t in _e4m3_table() if t[0] >= 0 and not (t[0] == 0 and t[1] == 128)]
+    vals = np.array([t[0] for t in table])
+    codes = np.array([t[1] for t in table])
+    rng = np.random.default_rng(31)
+    x = np.concatenate([rng.uniform(0, 500, 4000), rng.uniform(0, 0.05, 2000), 2.0 ** rng.uniform(-12, 9, 2000),
+                        (vals[:-1] + vals[1:]) / 2])                        # every midpoint: ties
+    got = uo.e4m3_round(x)
+    for xi, gi in zip(x, got):
+        d = np.abs(vals - min(xi, 448.0))
+        best = np.flatnonzero(d == d.min())
+        pick = best[0] if len(best) == 1 else best[np.argmin(codes[best] & 1)]   # tie: even mantissa
+        assert gi == vals[pick], (xi, gi, vals[pick])
+    np.testing.assert_array_equal(uo.e4m3_round(-x), -got)
+
+
+def test_e4m3_round_matches_torch_float8():
+    rng = np.random.default_rng(32)
+    x = np.concatenate([rng.standard_normal(20000) * 50, rng.standard_normal(5000) * 0.01])
+    x = x[np.abs(x) <= 464]                            # torch's cast turns larger values into NaN, not 448
+    x = x.astype(np.float32).astype(np.float64)        # torch rounds fp64 through fp32 first; feed fp32 values
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(uo.e4m3_round(x), ref)
+
+
+def test_quantize_e4m3_heads_against_torch_fp32_and_float8():
+    rng = np.random.default_rng(33)
+    T = (rng.standard_normal((2, 2, 2, 3, 10, 16)) * rng.uniform(0.1, 30, (1, 1, 2, 3, 1, 1))).astype(np.float32)
+    T[:, :, 1, 2] = 0.0                                # an all-zero head
+    codes, scales = uo.quantize_e4m3_heads(T)
+    t = torch.from_numpy(T)
+    amax = t.abs().amax(dim=(0, 1, 4, 5))
+    inv = torch.where(amax > 0, torch.tensor(448.0, dtype=torch.float32) / torch.where(amax > 0, amax, 1.0),
+                      torch.ones_like(amax))
+    ref = (t * inv[None, None, :, :, None, None]).to(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(codes, ref)
+    np.testing.assert_array_equal(scales, torch.where(amax > 0, amax / 448.0, 1.0).double().numpy())
+    assert np.all(np.abs(codes).max(axis=(0, 1, 4, 5))[amax.numpy() > 0] == 448.0)   # amax -> +-448
+    assert np.all(codes[:, :, 1, 2] == 0) and scales[1, 2] == 1.0
+    deq = codes * scales[None, None, :, :, None, None]
+    assert np.all(np.abs(deq - T) <= 2.0 ** -4 * np.abs(T) + 2.0 ** -10 * scales[None, None, :, :, None, None])
+    T2 = T.copy()
+    T2[:, :, 0, 0] *= 2                                # heads are independent
+    c2, _ = uo.quantize_e4m3_heads(T2)
+    mask = np.ones((2, 3), bool)
+    mask[0, 0] = False
+    np.testing.assert_array_equal(c2[:, :, mask], codes[:, :, mask])
+
+
+def test_usp_forward_fp8_equals_sdpa_of_dequantised():
+    u, r, B, H, N, D, scale = 2, 2, 1, 4, 32, 16, 0.25
+    q, k, v = (_rand((B, H, N, D), s) * f for s, f in ((170, 3.0), (171, 1.0), (172, 2.0)))
+    T = [wl.to_token_stack(x, u, r).numpy() for x in (q, k, v)]
+    O, L, codes, scales = uo.usp_forward_fp8(*T, u, r, scale)
+    deq = [wl.from_token_stack(torch.from_numpy(c * sc[None, None, :, :, None, None])) for c, sc in zip(codes, scales)]
+    ro, rl = _sdpa(*deq, scale)
+    np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(O)).numpy(), ro.numpy(), atol=1e-12)
+    np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(L)).numpy(), rl.numpy(), atol=1e-12)
+    # and it stays near unquantised attention (E4M3 keeps 3 mantissa bits)
+    eo, _ = _sdpa(q / 3, k, v, scale)
+    O2, _, _, _ = uo.usp_forward_fp8(wl.to_token_stack(q / 3, u, r).numpy(), T[1], T[2], u, r, scale)
+    assert np.abs(wl.from_token_stack(torch.from_numpy(O2)).numpy() - eo.numpy()).max() < 0.25
+
+
 # ----------------------------------------------------------------- backward
 
 def test_bwd_matches_autograd():
@@ -333,6 +419,22 @@ def _pins_pass(mod) -> bool:
         rc, _ = _sdpa(torch.from_numpy(q), torch.from_numpy(kt), torch.from_numpy(vt), 0.5)
         if not np.allclose(wl.from_token_stack(torch.from_numpy(Oc)).numpy(), rc.numpy(), atol=1e-10):
             return False
+        # FP8: rounding against torch's float8 cast, per-head quantisation, dequantised attention
+        xs = (rng.standard_normal(4000) * 60).astype(np.float32).astype(np.float64)
+        xs = xs[np.abs(xs) <= 464]
+        if not np.array_equal(mod.e4m3_round(xs), torch.from_numpy(xs).to(torch.float8_e4m3fn).double().numpy()):
+            return False
+        Tq8 = (T[0] * np.array([1.0, 7.0])[None, None, None, :, None, None]).astype(np.float32)
+        c8, s8 = mod.quantize_e4m3_heads(Tq8)
+        t8 = torch.from_numpy(Tq8)
+        am = t8.abs().amax(dim=(0, 1, 4, 5))
+        if not np.array_equal(c8, (t8 * (448.0 / am)[None, None, :, :, None, None]).to(torch.float8_e4m3fn).double().numpy()):
+            return False
+        O8, _, cq, sq = mod.usp_forward_fp8(*T, 2, 2, 0.5)
+        dq8 = [wl.from_token_stack(torch.from_numpy(c * sc[None, None, :, :, None, None])) for c, sc in zip(cq, sq)]
+        r8, _ = _sdpa(*dq8, 0.5)
+        if not np.allclose(wl.from_token_stack(torch.from_numpy(O8)).numpy(), r8.numpy(), atol=1e-10):
+            return False
         oo, ll = uo.attention(q, k, v, 0.5)
         do = rng.standard_normal(q.shape)
         qt, kt, vt = (torch.from_numpy(a).requires_grad_() for a in (q, k, v))
@@ -366,6 +468,10 @@ MUTATIONS = [
     ("    Xo, Xl = lse_merge(parts_o, parts_l)\n    out =", "    Xo, Xl = lse_merge(parts_o[:ring], parts_l[:ring])\n    out ="),  # text chunk dropped
     ("po[c], pl[c] = attention(qt[:, hs], Xk[c, j]", "po[c], pl[c] = attention(qt[:, hs], Xk[c, (j + 1) % ulysses]"),  # text queries, wrong head group
     ("O[g, j], L[g, j] = attention(Tq[g, j], kt", "O[g, j], L[g, j] = attention(Tq[g, (j + 1) % ulysses], kt"),  # cross: wrong rank's tokens
+    ("y = np.round(a / quantum) * quantum", "y = np.trunc(a / quantum) * quantum"),              # E4M3: truncation
+    ("E4M3_MAX = 448.0", "E4M3_MAX = 240.0"),                                                     # E4M3: wrong range
+    ("amax = np.abs(T32).max(axis=(0, 1, 4, 5))", "amax = np.abs(T32).max() + np.zeros(T32.shape[2:4], np.float32)"),  # one scale for all heads
+    ("deq = [c * sc[None, None, :, :, None, None] for c, sc in zip(codes, scales)]", "deq = [c for c in codes]"),  # no dequantisation
     ("dS = P * (dP - delta[..., None])", "dS = P * (dP + delta[..., None])"),                    # wrong sign
     ("dk = scale * (np.swapaxes(dS, -1, -2) @ q)", "dk = scale * (np.swapaxes(dS, -1, -2) @ k)"), # wrong operand
     ("dv = np.swapaxes(P, -1, -2) @ dout", "dv = P @ dout"),                                      # missing transpose
