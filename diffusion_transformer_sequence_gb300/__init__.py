@@ -6,12 +6,14 @@ The compute path lives in ``libusp.so`` (``csrc/``, declared in
 from .api import (  # noqa: F401
     attention_bwd,
     attention_fwd,
+    attention_fwd_fp8,
     attention_fwd_joint,
     attn_chunk_fwd,
     cross_attention_fwd,
     device_status,
     joint_workspace_bytes,
     lse_merge,
+    quantize_e4m3,
     relayout_head2tok,
     relayout_tok2head,
     set_spin_limit,

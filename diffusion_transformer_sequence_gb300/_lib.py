@@ -48,6 +48,10 @@ SIGNATURES = {
                                        _i64, _int, _int, _f32, _int, _int, _vp, _sz, _vp]),
     "usp_cross_attention_fwd": (_int, [_vp, _vp, _vp, _vp, _fp, _i64, _i64, _i64, _i64, _i64, _int, _int, _f32,
                                        _int, _vp]),
+    "usp_quantize_e4m3": (_int, [_vp, _vp, _fp, _i64, _i64, _i64, _i64, _int, _int, _vp]),
+    "usp_attention_fp8_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _int, _int]),
+    "usp_attention_fwd_fp8": (_int, [_vp, _vp, _vp, _vp, _fp, _i64, _i64, _i64, _i64, _int, _int, _f32, _vp, _sz,
+                                     _vp]),
     "usp_attention_fwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _fp, _i64, _i64, _i64, _i64, _int, _int, _f32, _int,
                                          _vp]),
     "usp_device_status": (_int, [_vp]),

@@ -229,6 +229,41 @@ def cross_attention_fwd(q, k_txt, v_txt, ulysses: int, ring: int, scale: float |
     return out, lse
 
 
+def quantize_e4m3(x, ulysses: int, ring: int):
+    """Per-head E4M3 codes (uint8, same stack layout) and dequantisation
+    scales [B, H] fp32 of a bf16 token-sharded stack."""
+    B, H, N, D = _stack_dims(x, ulysses, ring)
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, H), dtype=torch.float32, device=x.device)
+    _dev(x, x8, scales)
+    check("usp_quantize_e4m3", _lib.lib().usp_quantize_e4m3(
+        _p(x), _p(x8), _p(scales), B, H, N, D, ulysses, ring, _stream()))
+    return x8, scales
+
+
+def attention_fwd_fp8(q, k, v, ulysses: int, ring: int, scale: float | None = None, out=None, lse=None,
+                      workspace=None):
+    """FP8 (E4M3) fused USP forward of bf16 token-sharded stacks -> (out bf16, lse fp32)."""
+    host = not q.is_cuda
+    if host:
+        q, k, v = _to_device((q, k, v), torch.device("cuda", torch.cuda.current_device()))
+    B, H, N, D = _stack_dims(q, ulysses, ring)
+    scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty(q.shape[:5], dtype=torch.float32, device=q.device) if lse is None else lse
+    _dev(q, k, v, out, lse)
+    need = int(_lib.lib().usp_attention_fp8_workspace_bytes(B, H, N, D, ulysses, ring))
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    check("usp_attention_fwd_fp8", _lib.lib().usp_attention_fwd_fp8(
+        _p(q), _p(k), _p(v), _p(out), _p(lse), B, H, N, D, ulysses, ring, scale, _p(workspace) if need else None,
+        need, _stream()))
+    if host:
+        out, lse = _to_host(out), _to_host(lse)
+        torch.cuda.current_stream().synchronize()
+    return out, lse
+
+
 def attention_bwd(q, k, v, out, lse, dout, ulysses: int, ring: int, scale: float | None = None,
                   workspace=None):
     """USP attention backward over token-sharded stacks -> (dq, dk, dv)."""

@@ -565,6 +565,69 @@ int usp_cross_attention_fwd(const void* q, const void* k_txt, const void* v_txt,
   return run_attention(a, dtype, D, (cudaStream_t)stream);
 }
 
+int usp_quantize_e4m3(const void* x, void* x8, float* scales, int64_t B, int64_t H, int64_t N, int64_t D,
+                      int ulysses, int ring, usp_stream_t stream) {
+  if (B < 0 || H < 0 || N < 0 || D < 1 || ulysses < 1 || ring < 1) return USP_ERR_INVALID_ARG;
+  if (N % ((int64_t)ulysses * ring) != 0) return USP_ERR_DIVISIBILITY;
+  if (D % 16 != 0) return USP_ERR_UNSUPPORTED;
+  if (B * H == 0) return USP_OK;
+  if (!scales || (N > 0 && (!x || !x8))) return USP_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(scales, 4)) return USP_ERR_INVALID_ARG;
+  const int64_t sp = (int64_t)ulysses * ring, BH = B * H;
+  if (sp * BH > 65535) return USP_ERR_UNSUPPORTED;
+  // the scales buffer doubles as the amax scratch (converted in place)
+  cudaError_t e = launch_quantize_e4m3(x, static_cast<uint8_t*>(x8), scales, reinterpret_cast<unsigned*>(scales),
+                                       BH, sp, N / sp, D, (cudaStream_t)stream);
+  return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+
+size_t usp_attention_fp8_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring) {
+  if (check_dims(B, H, N, D, ulysses, ring) != USP_OK || D != 128) return 0;
+  const int64_t sp = (int64_t)ulysses * ring, Ns = N / sp, BH = B * H;
+  const size_t codes = round_up((size_t)(sp * BH * Ns * 128));
+  return 2 * codes + round_up((size_t)(sp * BH * 128 * fp8_vt_pitch(Ns))) + round_up((size_t)(3 * BH) * 4);
+}
+
+int usp_attention_fwd_fp8(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B, int64_t H,
+                          int64_t N, int64_t D, int ulysses, int ring, float scale, void* workspace,
+                          size_t workspace_bytes, usp_stream_t stream) {
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  if (D != 128) return USP_ERR_UNSUPPORTED;
+  if (B * H * N == 0) return USP_OK;
+  if (!q || !k || !v || !out || !lse) return USP_ERR_INVALID_ARG;
+  if (!(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) && aligned(lse, 4)))
+    return USP_ERR_INVALID_ARG;
+  const size_t need = usp_attention_fp8_workspace_bytes(B, H, N, D, ulysses, ring);
+  if (!workspace || workspace_bytes < need) return USP_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return USP_ERR_INVALID_ARG;
+  const int64_t sp = (int64_t)ulysses * ring, Ns = N / sp, BH = B * H, Ns_pad = fp8_vt_pitch(Ns);
+  if (BH > 65535 || sp * BH > 65535) return USP_ERR_UNSUPPORTED;
+  char* ws = static_cast<char*>(workspace);
+  const size_t codes = round_up((size_t)(sp * BH * Ns * 128));
+  uint8_t* q8 = reinterpret_cast<uint8_t*>(ws);
+  uint8_t* k8 = q8 + codes;
+  uint8_t* vt8 = k8 + codes;
+  unsigned* amax = reinterpret_cast<unsigned*>(vt8 + round_up((size_t)(sp * BH * 128 * Ns_pad)));
+  cudaStream_t s = (cudaStream_t)stream;
+  Guard g;
+  if ((st = guard(&g)) != USP_OK) return st;
+  phase_begin(s);
+  cudaError_t e = launch_quantize_qkv_fp8(q, k, v, q8, k8, vt8, amax, BH, sp, Ns, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  phase_mark(s);
+  Fp8AttnArgs a{};
+  a.q8 = q8; a.k8 = k8; a.vt8 = vt8; a.amax = amax;
+  a.out = out; a.lse = lse;
+  a.BH = BH; a.sp = sp; a.Ns = Ns; a.Ns_pad = Ns_pad;
+  a.scale = scale;
+  e = launch_attn_fp8_fwd(a, g, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  phase_mark(s);
+  return USP_OK;
+}
+
 int usp_attention_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
                       const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N, int64_t D,
                       int ulysses, int ring, float scale, usp_dtype dtype, void* workspace, size_t workspace_bytes,

@@ -130,6 +130,24 @@ cudaError_t launch_attn_f32(const AttnArgs& a, int D, cudaStream_t stream);
 // problems (same stack geometry and scale).
 cudaError_t launch_attn_tc_fwd(const AttnArgs* sides, int nsides, const Guard& g, cudaStream_t stream);
 
+// FP8 (E4M3) path: per-head quantisation of bf16 token stacks, then the fused
+// FP8 attention forward.
+int64_t fp8_vt_pitch(int64_t Ns);  // row pitch (bytes) of the transposed V codes: Ns rounded up to 16
+cudaError_t launch_quantize_e4m3(const void* x, uint8_t* x8, float* scales, unsigned* amax, int64_t BH, int64_t sp,
+                                 int64_t Ns, int64_t D, cudaStream_t stream);
+cudaError_t launch_quantize_qkv_fp8(const void* q, const void* k, const void* v, uint8_t* q8, uint8_t* k8,
+                                    uint8_t* vt8, unsigned* amax, int64_t BH, int64_t sp, int64_t Ns,
+                                    cudaStream_t stream);
+struct Fp8AttnArgs {
+  const uint8_t *q8, *k8, *vt8;  // [sp][BH][Ns][128], [sp][BH][Ns][128], [sp][BH][128][Ns_pad]
+  const unsigned* amax;          // [3][BH] float bits
+  void* out;                     // bf16 [sp][BH][Ns][128]
+  float* lse;                    // [sp][BH][Ns]
+  int64_t BH, sp, Ns, Ns_pad;
+  float scale;
+};
+cudaError_t launch_attn_fp8_fwd(const Fp8AttnArgs& a, const Guard& g, cudaStream_t stream);
+
 // bf16 tcgen05 backward over token-sharded stacks (D = 128): prep (Delta,
 // lse*log2e into workspace), dK/dV kernel, dQ kernel.
 struct TcBwdArgs {

@@ -208,6 +208,36 @@ int usp_cross_attention_fwd(const void* q, const void* k_txt, const void* v_txt,
                             int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t D, int ulysses, int ring,
                             float scale, usp_dtype dtype, usp_stream_t stream);
 
+/* FP8 (OCP E4M3) per-head quantisation ([HB] Wan latency table: "FP8 low
+ * precision" as the last latency step; the pages print no scheme, this is
+ * the plainest one).  x: bf16 token-sharded stack [ring, ulysses, B, H, Ns,
+ * D]; x8: uint8 codes in the same layout; scales: [B, H] fp32.  Per (b, h)
+ * head over every shard, token and dimension: amax = max |x|,
+ * code = e4m3(x * (448 / amax)) (fp32 multiply and divide, round to nearest
+ * even, saturating at +-448), scales = amax / 448; an all-zero head gets
+ * scale 1 and zero codes.  x must be finite.  D % 16 == 0; 16-byte aligned
+ * pointers.  Errors: INVALID_ARG, DIVISIBILITY, UNSUPPORTED, CUDA. */
+int usp_quantize_e4m3(const void* x, void* x8, float* scales, int64_t B, int64_t H, int64_t N, int64_t D,
+                      int ulysses, int ring, usp_stream_t stream);
+
+/* Bytes of workspace usp_attention_fwd_fp8 needs (0 for arguments it would
+ * reject): the E4M3 codes of q and k, the transposed codes of v (keys padded
+ * to a multiple of 16 per shard) and the per-head amax of all three. */
+size_t usp_attention_fp8_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring);
+
+/* FP8 fused USP attention forward.  q, k, v, out: bf16 token-sharded stacks
+ * as in usp_attention_fwd (D = 128); lse: fp32.  q, k and v are quantised
+ * per head as in usp_quantize_e4m3; Q K^T and P V run on the tensor cores
+ * in E4M3 with fp32 accumulation (P rounded to E4M3 for the product, its row
+ * sum kept in fp32); the softmax is fp32; the output is dequantised to bf16.
+ * The result approximates usp_attention_fwd; against attention of the
+ * dequantised q, k, v the remaining error is that of rounding P (bounded
+ * statistically, not element-wise).
+ * Errors: INVALID_ARG, DIVISIBILITY, UNSUPPORTED (D != 128), WORKSPACE, CUDA. */
+int usp_attention_fwd_fp8(const void* q, const void* k, const void* v, void* out, float* lse, int64_t B, int64_t H,
+                          int64_t N, int64_t D, int ulysses, int ring, float scale, void* workspace,
+                          size_t workspace_bytes, usp_stream_t stream);
+
 /* The materialised forward (same arguments, layouts, result and errors as
  * usp_attention_fwd with mode USP_MATERIALISED) for callers that cannot
  * allocate device memory: code running under a framework whose caching
@@ -236,6 +266,7 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
  *                         (the two kernels run concurrently; both phases
  *                         are timed from the end of the prep)
+ *   FP8 forward:          [quantise q, k, v] [FP8 attention]
  *   joint fused:          [attention: image and text queries, one launch]
  *   joint materialised:   [tok2head q,k,v] [partials against the image chunks
  *                         and against the text] [merge] [head2tok x2]

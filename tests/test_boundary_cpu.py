@@ -133,6 +133,27 @@ def test_cross_attention_validation(L):
     assert f(None, None, None, None, None, 1, 40, 0, 512, 128, 8, 2, 0.1, 1, None) == 0  # empty
 
 
+def test_fp8_validation_and_workspace(L):
+    q = L.usp_quantize_e4m3
+    assert q(FAKE, FAKE, FAKE, 1, 24, 4096, 120, 2, 2, None) == 3     # D % 16
+    assert q(FAKE, FAKE, FAKE, 1, 24, 4098, 128, 2, 2, None) == 2     # N % sp
+    assert q(FAKE + 8, FAKE, FAKE, 1, 24, 4096, 128, 2, 2, None) == 1  # misaligned
+    assert q(None, None, FAKE, 0, 24, 4096, 128, 2, 2, None) == 0     # empty
+    ws = L.usp_attention_fp8_workspace_bytes(1, 24, 4096, 128, 2, 2)
+    assert ws == 3 * (4 * 24 * 1024 * 128) + 512                       # q, k codes, V^T codes, amax (256-aligned)
+    # Ns = 4725 (Wan 720p, u8 x r2): V^T rows padded to 4736
+    assert L.usp_attention_fp8_workspace_bytes(1, 40, 75600, 128, 8, 2) == \
+        2 * ((16 * 40 * 4725 * 128 + 255) // 256 * 256) + (16 * 40 * 128 * 4736 + 255) // 256 * 256 + 512
+    assert L.usp_attention_fp8_workspace_bytes(1, 24, 4096, 64, 2, 2) == 0
+    f = L.usp_attention_fwd_fp8
+    a = (FAKE, FAKE, FAKE, FAKE, FAKE)
+    assert f(*a, 1, 24, 4096, 64, 2, 2, 0.1, None, 0, None) == 3       # D != 128
+    assert f(*a, 1, 24, 4096, 128, 2, 2, float("inf"), None, 0, None) == 1
+    assert f(*a, 1, 24, 4096, 128, 2, 2, 0.1, None, 0, None) == 4      # no workspace
+    assert f(*a, 1, 24, 4096, 128, 2, 2, 0.1, FAKE, ws - 1, None) == 4
+    assert f(*a, 1, 23, 4096, 128, 2, 2, 0.1, FAKE, ws, None) == 2     # H % ulysses
+
+
 def test_product_path_does_not_import_oracle():
     import subprocess
     import sys
