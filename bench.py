@@ -403,6 +403,36 @@ def time_rows(w, reps=10):
     T = torch.empty_like(q)
     t = timed(lambda: usp.relayout_head2tok(X, w.ulysses, w.ring, out=T))
     res["head2tok"] = {"GB/s": 2 * w.t_bytes / t / 1e9, "us": t * 1e6, "bytes": 2 * w.t_bytes}
+    if w.dtype == "bf16":
+        # the bandwidth-bound launches inside the materialised forward, as the step runs them:
+        # tok2head of q, k, v in one launch, the ring merge, head2tok of out and lse (phase events)
+        import ctypes
+        L = usp.lib()
+        kk, vv = torch.randn_like(q), torch.randn_like(q)
+        om, lm = torch.empty_like(q), torch.empty(w.lse_stack_shape, device="cuda")
+        wsm = torch.empty(usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, "materialised"),
+                          dtype=torch.uint8, device="cuda")
+        ms = (ctypes.c_float * 8)()
+        L.usp_profile_phases(1)
+        ph = []
+        for _ in range(reps + 2):
+            flush.fill_(1)
+            usp.attention_fwd(q, kk, vv, w.ulysses, w.ring, w.scale, mode="materialised", out=om, lse=lm,
+                              workspace=wsm)
+            n = L.usp_profile_read(ms, 8)
+            ph.append([ms[i] * 1e-3 for i in range(n)])
+        L.usp_profile_phases(0)
+        ph = ph[2:]
+        lse_b = w.B * w.H * w.N * 4
+        t_in = statistics.median(p_[0] for p_ in ph)
+        res["tok2head_qkv_in_step"] = {"GB/s": 6 * w.t_bytes / t_in / 1e9, "us": t_in * 1e6, "bytes": 6 * w.t_bytes}
+        if w.ring > 1:
+            t_m = statistics.median(p_[2] for p_ in ph)
+            byt = (w.ring + 1) * (w.t_bytes + lse_b)
+            res["lse_merge_in_step"] = {"GB/s": byt / t_m / 1e9, "us": t_m * 1e6, "bytes": byt}
+        t_out = statistics.median(p_[3] for p_ in ph)
+        byt = 2 * (w.t_bytes + lse_b)
+        res["head2tok_out_lse_in_step"] = {"GB/s": byt / t_out / 1e9, "us": t_out * 1e6, "bytes": byt}
     if w.Nt:
         # cross-attention of the sharded image queries to the replicated text K/V (tensor-bound:
         # reported as TFLOP/s beside its bytes)
@@ -414,6 +444,33 @@ def time_rows(w, reps=10):
         flop = 4.0 * w.B * w.H * w.N * w.Nt * w.D
         byt = 2 * w.t_bytes + w.B * w.H * w.N * 4 + 2 * kt.numel() * kt.element_size()
         res["cross_attention"] = {"GB/s": byt / t / 1e9, "us": t * 1e6, "bytes": byt, "TFLOP/s": flop / t / 1e12}
+    if w.dtype == "bf16" and not w.Nt:
+        # FP8 (E4M3) fused forward of the same stacks: quantise q, k, v + FP8 attention (bf16-equivalent
+        # FLOP rate), with the two phases timed separately
+        import ctypes
+        L = usp.lib()
+        k_ = torch.randn(w.stack_shape, device="cuda").to(w.torch_dtype)
+        v_ = torch.randn(w.stack_shape, device="cuda").to(w.torch_dtype)
+        o = torch.empty_like(q)
+        l = torch.empty(w.lse_stack_shape, device="cuda")
+        ws8 = torch.empty(int(L.usp_attention_fp8_workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring)),
+                          dtype=torch.uint8, device="cuda")
+        t = timed(lambda: usp.attention_fwd_fp8(q, k_, v_, w.ulysses, w.ring, w.scale, out=o, lse=l, workspace=ws8))
+        ms = (ctypes.c_float * 8)()
+        L.usp_profile_phases(1)
+        ph = []
+        for _ in range(reps):
+            flush.fill_(1)
+            usp.attention_fwd_fp8(q, k_, v_, w.ulysses, w.ring, w.scale, out=o, lse=l, workspace=ws8)
+            n = L.usp_profile_read(ms, 8)
+            ph.append([ms[i] * 1e-3 for i in range(n)])
+        L.usp_profile_phases(0)
+        tq = statistics.median(p_[0] for p_ in ph)
+        ta = statistics.median(p_[1] for p_ in ph)
+        qbytes = 3 * 2 * w.t_bytes + 3 * w.t_bytes // 2          # amax pass + quantise pass read, codes written
+        res["fp8_quantise"] = {"GB/s": qbytes / tq / 1e9, "us": tq * 1e6, "bytes": qbytes}
+        res["fp8_fwd"] = {"us": t * 1e6, "TFLOP/s": w.fwd_flop / t / 1e12, "attention_us": ta * 1e6,
+                          "attention_TFLOP/s": w.fwd_flop / ta / 1e12}
     if w.ring > 1:
         R = w.ring
         outs = torch.randn((R, w.B, w.H, w.N, w.D), device="cuda").to(w.torch_dtype)
@@ -521,7 +578,8 @@ def our_arm(args, w, ws, rank, local):
                 "launch_ms": t_dom * 1e3, "algorithmic_flop_per_launch": f_dom,
                 "peak_kind": f"bf16 dense burst, {peaks['source']} (sustained {peaks['bf16_tflops_sustained']})"}
     for k, r in rows.items():
-        r["frac_of_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
+        if "GB/s" in r:
+            r["frac_of_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
     cpu = None
     if not args.no_cpu_baseline:
         heads = sample_heads(w)
@@ -549,9 +607,10 @@ def our_arm(args, w, ws, rank, local):
                  **({k + "_ms": v[0] * 1e3 for k, v in kernels.items()}),
                  **({k + "_tflops": v[1] / v[0] / 1e12 for k, v in kernels.items()}),
                  **overlapped,
-                 **{k + "_GBps": v["GB/s"] for k, v in rows.items()},
+                 **{k + "_GBps": v["GB/s"] for k, v in rows.items() if "GB/s" in v},
                  **{k + "_tflops": v["TFLOP/s"] for k, v in rows.items() if "TFLOP/s" in v},
-                 **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items()}},
+                 **({"fp8_attention_kernel_tflops": rows["fp8_fwd"]["attention_TFLOP/s"]} if "fp8_fwd" in rows else {}),
+                 **{k + "_frac_hbm": v["frac_of_hbm"] for k, v in rows.items() if "frac_of_hbm" in v}},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

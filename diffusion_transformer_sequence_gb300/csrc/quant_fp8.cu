@@ -15,9 +15,10 @@
 //                  (non-negative floats order like their bit patterns)
 //   quant_kernel   16 elements per thread, codes in the input layout
 //   quant_vt_kernel  V for the P V product: 128-key x 128-dim tiles staged
-//                  through shared memory and written transposed, [D][Ns_pad]
-//                  per (shard, head) with zero padding, so V^T tiles are
-//                  K-major operands (keys contiguous) for the tensor cores.
+//                  through shared memory (4 keys per 32-bit word) and written
+//                  transposed, [D][Ns_pad] per (shard, head) with zero
+//                  padding, so V^T tiles are K-major operands (keys
+//                  contiguous) for the tensor cores.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -101,41 +102,57 @@ __global__ void __launch_bounds__(kThreads) quant_kernel(Srcs3 srcs, Dsts3 dsts,
 }
 
 // V^T: for each (s, bh) and 128-key tile, dst[s][bh][d][key] (row pitch Ns_pad).
-constexpr int kVtPitch = 144;  // bytes per d-row in shared memory (128 keys + 16: 16-byte aligned, fewer conflicts)
-
+// A thread reads 4 consecutive keys x 8 dims (16 lanes cover one 256-byte
+// key row, so loads are coalesced) and packs, per dim, the 4 keys' codes into
+// one 32-bit word of a shared [128 d][32 words] tile; word column kq of row d
+// sits at kq ^ 4*((d/8) % 8), which limits the stores to 2-way bank conflicts
+// and keeps each 16-byte group of 16 keys contiguous for the write-out.
 __global__ void __launch_bounds__(kThreads) quant_vt_kernel(const __nv_bfloat16* __restrict__ v,
                                                             uint8_t* __restrict__ vt,
                                                             const unsigned* __restrict__ amax_v, int64_t BH,
                                                             int64_t Ns, int64_t Ns_pad) {
-  __shared__ __align__(16) uint8_t tile[128 * kVtPitch];
+  __shared__ __align__(16) uint32_t tile[128 * 32];
   const int64_t key0 = (int64_t)blockIdx.x * 128;
   const int64_t bh = blockIdx.y, s = blockIdx.z;
   const float inv = inv_scale(__ldg(amax_v + bh));
   const __nv_bfloat16* src = v + ((s * BH + bh) * Ns) * 128;
-  // load [128 keys][128 d]: 2048 vectors of 8 bf16, 8 per thread; write transposed bytes
-  for (int i = threadIdx.x; i < 128 * 16; i += kThreads) {
-    const int kr = i / 16, d0 = (i % 16) * 8;
-    uint32_t w[4] = {0u, 0u, 0u, 0u};
-    if (key0 + kr < Ns) {
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + (key0 + kr) * 128 + d0));
-      w[0] = raw.x; w[1] = raw.y; w[2] = raw.z; w[3] = raw.w;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int dq = lane % 16, d0 = 8 * dq;
+  const int sw = 4 * (dq & 7);
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+    const int kq = pass * 16 + warp * 2 + lane / 16;  // keys 4kq .. 4kq+3 of the tile
+    uint32_t w[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int64_t key = key0 + 4 * kq + r;
+      if (key < Ns) {
+        const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src + key * 128 + d0));
+        w[r][0] = raw.x; w[r][1] = raw.y; w[r][2] = raw.z; w[r][3] = raw.w;
+      } else {
+        w[r][0] = w[r][1] = w[r][2] = w[r][3] = 0u;
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float x0 = __fmul_rn(__uint_as_float(w[j] << 16), inv);
-      const float x1 = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), inv);
-      const uint16_t c = ptx::e4m3x2(x0, x1);
-      tile[(d0 + 2 * j) * kVtPitch + kr] = (uint8_t)(c & 0xFF);
-      tile[(d0 + 2 * j + 1) * kVtPitch + kr] = (uint8_t)(c >> 8);
+    for (int dd = 0; dd < 8; ++dd) {
+      float x[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const uint32_t h = w[r][dd / 2];
+        x[r] = __fmul_rn(__uint_as_float((dd & 1) ? (h & 0xFFFF0000u) : (h << 16)), inv);
+      }
+      tile[(d0 + dd) * 32 + (kq ^ sw)] = (uint32_t)ptx::e4m3x2(x[0], x[1]) | ((uint32_t)ptx::e4m3x2(x[2], x[3]) << 16);
     }
   }
   __syncthreads();
   uint8_t* dst = vt + ((s * BH + bh) * 128) * Ns_pad;
   for (int i = threadIdx.x; i < 128 * 8; i += kThreads) {
-    const int d = i / 8, c = i % 8;
+    const int d = i / 8, c = i % 8;                  // 16 keys [16c, 16c + 16) of dim row d
     const int64_t k = key0 + 16 * c;
-    if (k < Ns_pad)
-      *reinterpret_cast<uint4*>(dst + d * Ns_pad + k) = *reinterpret_cast<const uint4*>(tile + d * kVtPitch + 16 * c);
+    if (k < Ns_pad) {
+      const uint4 val = *reinterpret_cast<const uint4*>(tile + d * 32 + 4 * (c ^ ((d >> 3) & 7)));
+      *reinterpret_cast<uint4*>(dst + d * Ns_pad + k) = val;
+    }
   }
 }
 
