@@ -325,28 +325,84 @@ class Step:
                                  self.ws_b.data_ptr(), self.ws_b.numel(), torch.cuda.current_stream().cuda_stream)
         _lib.check("usp_attention_bwd", rc)
 
-    def run_e2e(self):
-        """Host buffers in and out: H2D of q, k, v, the step, D2H of the outputs."""
-        usp, w = self.usp, self.w
-        for n in self.inputs():
-            if n != "dout":
-                self.dev[n].copy_(self.host[n], non_blocking=True)
-        self.fwd("materialised")
-        self.fwd("fused")
+    def _out_names(self):
+        names = ["out_m", "lse_m", "out_f", "lse_f"]
+        return names + (["grads"] if self.backward else [])
+
+    def _swap_set(self, k):
+        """Point the step at buffer set k (0 or 1) of the pipelined end-to-end loop."""
+        if not hasattr(self, "_sets"):
+            own = {"dev": self.dev, **{n: getattr(self, n) for n in self._out_names()}}
+            if self.joint:
+                own["txt_out"] = self.txt_out
+            clone = lambda t: [x.clone() for x in t] if isinstance(t, list) else t.clone()
+            other = {"dev": {n: t.clone() for n, t in self.dev.items()},
+                     **{n: clone(getattr(self, n)) for n in self._out_names()}}
+            if self.joint:
+                other["txt_out"] = {m: tuple(x.clone() for x in v) for m, v in self.txt_out.items()}
+            self._sets = [own, other]
+        for n, v in self._sets[k].items():
+            setattr(self, n, v)
+
+    def _outputs(self):
         outs = [("out_m", self.out_m), ("lse_m", self.lse_m), ("out_f", self.out_f), ("lse_f", self.lse_f)]
         if self.joint:
             outs += [("ot_m", self.txt_out["m"][0]), ("lt_m", self.txt_out["m"][1]),
                      ("ot_f", self.txt_out["f"][0]), ("lt_f", self.txt_out["f"][1])]
         if self.backward:
-            self.dev["dout"].copy_(self.host["dout"], non_blocking=True)
-            self.bwd()
             outs += [("dq", self.grads[0]), ("dk", self.grads[1]), ("dv", self.grads[2])]
-        for name, t in outs:
-            dst = getattr(self, "h_" + name, None)
-            if dst is None:
-                dst = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                setattr(self, "h_" + name, dst)
-            dst.copy_(t, non_blocking=True)
+        return outs
+
+    def run_e2e_pipelined(self, steps):
+        """End to end with host buffers, software-pipelined over three streams:
+        step i's host->device copy of its inputs (pinned), its compute (L2
+        flushed first, as in the device-timed loop) and the device->host copy
+        of its results run on separate streams with two device buffer sets,
+        so step i+1's inputs arrive and step i-1's results leave while step i
+        computes.  Every step still moves its own inputs in and results out.
+        Returns the elapsed seconds from before the first copy to after the
+        last result has landed in host memory."""
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        s_cmp = torch.cuda.current_stream()
+        ev = lambda: torch.cuda.Event()
+        in_ready, done, out_free = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(s_cmp)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        host_out = {}
+        for i in range(steps):
+            k = i % 2
+            self._swap_set(k)
+            if i >= 2:
+                s_in.wait_event(done[k])              # step i-2 has finished reading set k
+            with torch.cuda.stream(s_in):
+                for n in self.inputs():
+                    self.dev[n].copy_(self.host[n], non_blocking=True)
+                in_ready[k].record(s_in)
+            s_cmp.wait_event(in_ready[k])
+            if i >= 2:
+                s_cmp.wait_event(out_free[k])         # step i-2's results have left set k
+            self.flush()
+            self.fwd("materialised")
+            self.fwd("fused")
+            if self.backward:
+                self.bwd()
+            done[k].record(s_cmp)
+            s_out.wait_event(done[k])
+            with torch.cuda.stream(s_out):
+                for name, t in self._outputs():
+                    dst = host_out.get(name)
+                    if dst is None:
+                        dst = host_out[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    dst.copy_(t, non_blocking=True)
+                out_free[k].record(s_out)
+        end.record(s_out)
+        end.synchronize()
+        s_cmp.wait_stream(s_out)
+        self._swap_set(0)
+        return start.elapsed_time(end) * 1e-3
 
     def inputs(self):
         names = ["q", "k", "v"] + (["dout"] if self.backward else [])
@@ -529,20 +585,14 @@ def our_arm(args, w, ws, rank, local):
     # end to end through the public call with host buffers
     e2e = None
     if not args.no_e2e and args.only is None:
-        for _ in range(2):
-            step.run_e2e()
-        torch.cuda.synchronize()
+        step.run_e2e_pipelined(max(3, args.warmup))      # warm-up, also allocates the second buffer set
         barrier(ws)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(args.steps):
-            step.run_e2e()
-        b.record()
-        torch.cuda.synchronize()
-        e2e_s = max_over_ranks(a.elapsed_time(b) * 1e-3 / args.steps, ws)
+        e2e_s = max_over_ranks(step.run_e2e_pipelined(args.steps) / args.steps, ws)
         h2d, d2h = step.io_bytes()
         e2e = {"value": ws * step.flop() / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+               "how": "pinned host buffers; per step H2D of the inputs, the step (L2 flushed first) and D2H of "
+                      "every result on three streams, two device buffer sets (steps overlap)"}
 
     rows = time_rows(w) if (rank == 0 and not args.no_rows) else {}
     if rank != 0:
