@@ -176,3 +176,42 @@ def test_bounded_wait_timeout_path():
     assert usp.device_status() == 0
     ro, rl = oracle.attention(f64(q), f64(k), f64(v), 1 / math.sqrt(D))
     check_out(o, l, ro, rl, "bf16", "after timeout")
+
+
+@pytest.mark.parametrize("path", ["backward", "fp8"])
+def test_bounded_wait_timeout_other_kernels(path):
+    """The same expiring-wait check for the backward kernels (dK/dV, and dQ on
+    the side stream) and the FP8 forward: error status, no hang, a cleared
+    status, and correct results on the next call."""
+    usp = _api()
+    w = wl.custom("to", "bf16", 1, 2, 512, 128, 2, 2, seed=8, backward=True)
+    inp = wl.make_inputs(w)
+    st = {n: wl.to_token_stack(t, 2, 2).cuda() for n, t in inp.items()}
+    o, l = usp.attention_fwd(st["q"], st["k"], st["v"], 2, 2, w.scale, mode="fused")
+    assert usp.device_status() == 0
+
+    def call():
+        if path == "fp8":
+            return usp.attention_fwd_fp8(st["q"], st["k"], st["v"], 2, 2, w.scale)
+        return usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+
+    try:
+        usp.set_spin_limit(0)
+        call()
+        status = usp.device_status()
+    finally:
+        usp.set_spin_limit(-1)
+    assert status == 6, f"expected USP_ERR_TIMEOUT, got {status}"
+    assert usp.device_status() == 0          # cleared
+    res = call()
+    assert usp.device_status() == 0
+    stacks = [f64(wl.to_token_stack(inp[n], 2, 2)) for n in ("q", "k", "v")]
+    if path == "fp8":
+        ro, _, _, _ = oracle.usp_forward_fp8(*stacks, 2, 2, w.scale)
+        assert np.abs(f64(res[0]) - ro).max() < 5e-2
+    else:
+        ro, rl = oracle.attention(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), w.scale)
+        rdq, _, _ = oracle.attention_bwd(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), ro, rl, f64(inp["dout"]),
+                                         w.scale)
+        got = f64(wl.from_token_stack(res[0].cpu()))
+        assert np.abs(got - rdq).max() / np.abs(rdq).max() < 2e-2
