@@ -489,6 +489,38 @@ def time_rows(w, reps=10):
         t_out = statistics.median(p_[3] for p_ in ph)
         byt = 2 * (w.t_bytes + lse_b)
         res["head2tok_out_lse_in_step"] = {"GB/s": byt / t_out / 1e9, "us": t_out * 1e6, "bytes": byt}
+    if w.dtype == "bf16" and not w.Nt:
+        # the backward through the materialised Ulysses path (tok2head of q, k, v, O, dO and lse,
+        # the per-rank chunk backward over the head-sharded stacks, head2tok of dq, dk, dv),
+        # timed whole and by phase
+        import ctypes
+        L = usp.lib()
+        k_ = torch.randn(w.stack_shape, device="cuda").to(w.torch_dtype)
+        v_ = torch.randn(w.stack_shape, device="cuda").to(w.torch_dtype)
+        do = torch.randn(w.stack_shape, device="cuda").to(w.torch_dtype)
+        o, l = usp.attention_fwd(q, k_, v_, w.ulysses, w.ring, w.scale, mode="fused")
+        wsb = torch.empty(usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, "materialised",
+                                              backward=True), dtype=torch.uint8, device="cuda")
+        t = timed(lambda: usp.attention_bwd(q, k_, v_, o, l, do, w.ulysses, w.ring, w.scale, workspace=wsb,
+                                            mode="materialised"))
+        ms = (ctypes.c_float * 8)()
+        L.usp_profile_phases(1)
+        ph = []
+        for _ in range(reps):
+            flush.fill_(1)
+            usp.attention_bwd(q, k_, v_, o, l, do, w.ulysses, w.ring, w.scale, workspace=wsb, mode="materialised")
+            n = L.usp_profile_read(ms, 8)
+            ph.append([ms[i] * 1e-3 for i in range(n)])
+        L.usp_profile_phases(0)
+        lse_b = w.B * w.H * w.N * 4
+        t_in = statistics.median(p_[0] for p_ in ph)
+        t_out = statistics.median(p_[-1] for p_ in ph)
+        res["bwd_materialised"] = {"us": t * 1e6, "TFLOP/s": w.bwd_flop / t / 1e12}
+        byt = 2 * (5 * w.t_bytes + lse_b)
+        res["bwd_tok2head_qkvodo_lse_in_step"] = {"GB/s": byt / t_in / 1e9, "us": t_in * 1e6, "bytes": byt}
+        byt = 2 * 3 * w.t_bytes
+        res["bwd_head2tok_grads_in_step"] = {"GB/s": byt / t_out / 1e9, "us": t_out * 1e6, "bytes": byt}
+        del k_, v_, do, o, l, wsb
     if w.Nt:
         # cross-attention of the sharded image queries to the replicated text K/V (tensor-bound:
         # reported as TFLOP/s beside its bytes)

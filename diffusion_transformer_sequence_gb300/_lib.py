@@ -43,6 +43,8 @@ SIGNATURES = {
                                  _vp, _sz, _vp]),
     "usp_attention_bwd": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int,
                                  _f32, _int, _vp, _sz, _vp]),
+    "usp_attention_bwd_materialised": (_int, [_vp, _vp, _vp, _vp, _fp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64,
+                                              _int, _int, _f32, _int, _vp, _sz, _vp]),
     "usp_attention_joint_workspace_bytes": (_sz, [_i64, _i64, _i64, _i64, _i64, _int, _int, _int, _int, _int]),
     "usp_attention_fwd_joint": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _fp, _vp, _fp, _i64, _i64, _i64, _i64,
                                        _i64, _int, _int, _f32, _int, _int, _vp, _sz, _vp]),

@@ -265,8 +265,14 @@ def attention_fwd_fp8(q, k, v, ulysses: int, ring: int, scale: float | None = No
 
 
 def attention_bwd(q, k, v, out, lse, dout, ulysses: int, ring: int, scale: float | None = None,
-                  workspace=None):
-    """USP attention backward over token-sharded stacks -> (dq, dk, dv)."""
+                  workspace=None, mode: str = "fused"):
+    """USP attention backward over token-sharded stacks -> (dq, dk, dv).
+
+    mode "fused" reads the stacks in place; "materialised" re-lays q, k, v,
+    O, dO and lse out head-sharded, runs the per-rank chunk backward there
+    and re-lays the gradients back (usp_attention_bwd_materialised)."""
+    if mode not in ("fused", "materialised"):
+        raise ValueError("mode must be 'fused' or 'materialised'")
     host = not q.is_cuda
     if host:
         q, k, v, out, lse, dout = _to_device((q, k, v, out, lse, dout),
@@ -275,10 +281,11 @@ def attention_bwd(q, k, v, out, lse, dout, ulysses: int, ring: int, scale: float
     scale = 1.0 / math.sqrt(D) if scale is None else float(scale)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     _dev(q, k, v, out, lse, dout, dq, dk, dv)
-    need = workspace_bytes(B, H, N, D, ulysses, ring, q.dtype, "fused", backward=True)
+    need = workspace_bytes(B, H, N, D, ulysses, ring, q.dtype, mode, backward=True)
     if need and (workspace is None or workspace.numel() < need):
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    check("usp_attention_bwd", _lib.lib().usp_attention_bwd(
+    name = "usp_attention_bwd" if mode == "fused" else "usp_attention_bwd_materialised"
+    check(name, getattr(_lib.lib(), name)(
         _p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv), B, H, N, D, ulysses, ring,
         scale, _dt(q), _p(workspace) if need else None, need, _stream()))
     if host:

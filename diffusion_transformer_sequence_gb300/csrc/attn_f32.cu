@@ -20,18 +20,22 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kTileK = 32;
 
+// Stack addressing [segments][BH][Ns][D]: a unit ("head") h in [0, useg*BH)
+// is (j, bh) = (h / BH, h % BH) and its k-th Ns-row segment is k*useg + j
+// (the token-sharded stack: useg = 1; the materialised path's head-sharded
+// stack [r*u][B*Hu][Nr][D]: useg = u).
 struct F32Addr {
   bool fused;
-  int64_t BH, Ns;  // fused: stack [sp][BH][Ns][D]
-  __device__ __forceinline__ int64_t row_off(int64_t head, int64_t row, int64_t nrows, int D) const {
-    if (!fused) return (head * nrows + row) * (int64_t)D;
-    const int64_t s = row / Ns, n = row - s * Ns;
-    return ((s * BH + head) * Ns + n) * (int64_t)D;
-  }
+  int64_t BH, Ns;
+  int64_t useg = 1;
   __device__ __forceinline__ int64_t lse_off(int64_t head, int64_t row, int64_t nrows) const {
     if (!fused) return head * nrows + row;
+    const int64_t j = head / BH, bh = head - j * BH;
     const int64_t s = row / Ns, n = row - s * Ns;
-    return (s * BH + head) * Ns + n;
+    return ((s * useg + j) * BH + bh) * Ns + n;
+  }
+  __device__ __forceinline__ int64_t row_off(int64_t head, int64_t row, int64_t nrows, int D) const {
+    return lse_off(head, row, nrows) * (int64_t)D;
   }
 };
 
@@ -264,13 +268,13 @@ cudaError_t launch_bwd_dmax(const float* q, const float* k, const float* v, cons
 
 cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, const float* out,
                                 const float* lse, const float* dout, float* dq, float* dk, float* dv,
-                                float* delta, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
+                                float* delta, int64_t BH, int64_t sp, int64_t Ns, int useg, int D, float scale,
                                 cudaStream_t stream) {
-  F32Addr addr{true, BH, Ns};
-  const int64_t N = sp * Ns;
-  if (D <= 32) return launch_bwd_dmax<32>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
-  if (D <= 64) return launch_bwd_dmax<64>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
-  return launch_bwd_dmax<128>(q, k, v, out, lse, dout, dq, dk, dv, delta, BH, N, D, scale, addr, stream);
+  F32Addr addr{true, BH, Ns, useg};
+  const int64_t N = sp / useg * Ns, U = BH * useg;  // rows per unit, units
+  if (D <= 32) return launch_bwd_dmax<32>(q, k, v, out, lse, dout, dq, dk, dv, delta, U, N, D, scale, addr, stream);
+  if (D <= 64) return launch_bwd_dmax<64>(q, k, v, out, lse, dout, dq, dk, dv, delta, U, N, D, scale, addr, stream);
+  return launch_bwd_dmax<128>(q, k, v, out, lse, dout, dq, dk, dv, delta, U, N, D, scale, addr, stream);
 }
 
 cudaError_t launch_attn_f32(const AttnArgs& a, int D, cudaStream_t stream) {

@@ -48,10 +48,11 @@ struct BwdParams {
   void* dst1;          // dkdv: dV   | dq: unused
   const float* l2;     // lse * log2(e), [sp][BH][Ns]
   const float* delta;  // rowsum(dO * O), [sp][BH][Ns]
-  int64_t BH, Ns;
+  int64_t BH, Ns;      // heads and rows per segment of the tensor maps
   int64_t Ns_pad;      // row pitch of l2 / delta (Ns rounded up to 4: 16-byte rows for TMA)
   int tiles_per_seg;
-  int tiles;           // tiles per head (sp * tiles_per_seg)
+  int tiles;           // tiles per unit (segments of the unit * tiles_per_seg)
+  int useg;            // segment stride: the unit's k-th segment is k * useg + j (j = unit / BH)
   float scale, scale_log2;
   Guard guard;
 };
@@ -59,10 +60,15 @@ struct BwdParams {
 struct TileRef {
   int row0, seg, valid;
 };
-__device__ __forceinline__ TileRef tile_ref(const BwdParams& p, int tile) {
+// Tile `tile` of the unit whose segment offset is j: the token-sharded stack
+// (useg = 1, j = 0) has every segment (virtual rank) of head bh; the
+// head-sharded stack of the materialised path (segments g*u + j, u = useg)
+// has the ring chunks g of Ulysses group j.
+__device__ __forceinline__ TileRef tile_ref(const BwdParams& p, int tile, int j) {
   TileRef t;
-  t.seg = tile / p.tiles_per_seg;
-  t.row0 = (tile - t.seg * p.tiles_per_seg) * BM;
+  const int k = tile / p.tiles_per_seg;
+  t.seg = k * p.useg + j;
+  t.row0 = (tile - k * p.tiles_per_seg) * BM;
   const int64_t rem = p.Ns - t.row0;
   t.valid = rem < BM ? (int)rem : BM;
   return t;
@@ -208,8 +214,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_ABORT);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t bh = blockIdx.y;
-  const TileRef kt = tile_ref(p, blockIdx.x);
+  const int jseg = (int)(blockIdx.y / p.BH);
+  const int64_t bh = blockIdx.y - (int64_t)jseg * p.BH;
+  const TileRef kt = tile_ref(p, blockIdx.x, jseg);
   const Guard& G = p.guard;
   const uint32_t tmem = prologue(smem, sbase, warp);
   const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int s = i % STAGES;
         const uint32_t ph = (uint32_t)((i / STAGES) & 1);
         if (!ptx::mbar_wait(bar(B_EMPTY + s), ph ^ 1u, G, abort_flag, kDevTimeoutTmaProducer)) break;
-        const TileRef qt = tile_ref(p, i);
+        const TileRef qt = tile_ref(p, i, jseg);
         const uint32_t st = stage_addr(sbase, s);
         ptx::mbar_arrive_expect_tx(bar(B_FULL + s), 2 * TILE_BYTES + 2 * VEC_BYTES);
         load_tile(&tm_q, st, bar(B_FULL + s), bh, qt);
@@ -401,8 +408,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + DQ_OFF_BAR + 8 * i; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_ABORT);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int64_t bh = blockIdx.y;
-  const TileRef qt = tile_ref(p, blockIdx.x);
+  const int jseg = (int)(blockIdx.y / p.BH);
+  const int64_t bh = blockIdx.y - (int64_t)jseg * p.BH;
+  const TileRef qt = tile_ref(p, blockIdx.x, jseg);
   const Guard& G = p.guard;
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(Q_RES), 1);
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int issued_k = 0, issued_v = 0;
       // K runs ahead of V by up to one slot: issue in the order the MMAs consume
       for (int j = 0; j < T; ++j) {
-        const TileRef kt = tile_ref(p, j);
+        const TileRef kt = tile_ref(p, j, jseg);
         const int sk = j % KSLOTS, sv = j % VSLOTS;
         if (!ptx::mbar_wait(bar(Q_KEMPTY + sk), (uint32_t)(((j / KSLOTS) & 1) ^ 1), G, abort_flag,
                             kDevTimeoutTmaProducer))
@@ -548,7 +556,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tmem_ld64(tS + lane_bits + c0, r);
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar(Q_SFREE));      // S(j) may now be overwritten
-      const int valid = tile_ref(p, j).valid - c0;  // key columns of this warpgroup that exist
+      const int valid = tile_ref(p, j, jseg).valid - c0;  // key columns of this warpgroup that exist
       if (valid < 64) {
 #pragma unroll
         for (int c = 0; c < 64; ++c)
@@ -696,11 +704,12 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   p.Ns = a.Ns;
   p.Ns_pad = Ns_pad;
   p.tiles_per_seg = (int)((a.Ns + BM - 1) / BM);
-  p.tiles = (int)(p.tiles_per_seg * a.sp);
+  p.useg = a.useg;
+  p.tiles = (int)(p.tiles_per_seg * (a.sp / a.useg));
   p.scale = a.scale;
   p.scale_log2 = a.scale * LOG2E;
   p.guard = g;
-  dim3 grid((unsigned)p.tiles, (unsigned)a.BH, 1);
+  dim3 grid((unsigned)p.tiles, (unsigned)(a.BH * a.useg), 1);
   // The two kernels are independent (each writes its own gradients): dQ runs
   // on the device's side stream, so its CTAs fill the dK/dV kernel's last,
   // partial wave instead of waiting behind it.

@@ -22,11 +22,13 @@ constexpr int kUnroll = 4;
 template <typename Vec>
 __device__ __forceinline__ Vec load_stream(const Vec* p) { return __ldg(p); }
 
-// Up to three tensors of the same shape per launch (blockIdx.z picks one):
-// q, k and v of the materialised forward go through one launch.
+// Up to five tensors of the same shape per launch (blockIdx.z picks one):
+// q, k and v of the materialised forward (and q, k, v, O, dO of the
+// materialised backward) go through one launch.
+constexpr int kMaxTensors = 5;
 struct Tensors {
-  const void* src[3];
-  void* dst[3];
+  const void* src[kMaxTensors];
+  void* dst[kMaxTensors];
 };
 
 template <typename Vec, bool kTok2Head>
@@ -95,7 +97,7 @@ cudaError_t launch_vec(const Tensors& ts, int count, int64_t nruns, int64_t run_
 cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
                               int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                               cudaStream_t stream) {
-  if (count < 1 || count > 3) return cudaErrorInvalidValue;
+  if (count < 1 || count > kMaxTensors) return cudaErrorInvalidValue;
   const int64_t u = ulysses;
   const int64_t Hu = H / u;
   const int64_t nruns = (int64_t)ring * u * B * H;

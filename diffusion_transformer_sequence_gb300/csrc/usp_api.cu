@@ -127,6 +127,35 @@ size_t bwd_vec_bytes(int64_t B, int64_t H, int64_t N, int u, int r) {
   return round_up((size_t)(sp * B * H * ((Ns + 3) / 4 * 4)) * 4);
 }
 
+// Materialised backward: head-sharded copies of q, k, v, O, dO, lse, the
+// head-sharded gradients, and the Delta / lse*log2(e) vectors of the kernels
+// over the head-sharded stack viewed as [r*u][B*Hu][Nr] (rows padded to 4).
+struct BwdWorkspace {
+  size_t xq, xk, xv, xo, xdo, xl, xdq, xdk, xdv, delta, l2, total;
+};
+BwdWorkspace bwd_layout(int64_t B, int64_t H, int64_t N, int64_t D, int u, int r, usp_dtype dt) {
+  const size_t t = round_up((size_t)(B * H * N * D) * elt_size(dt));
+  const size_t lb = round_up((size_t)(B * H * N) * 4);
+  const int64_t Nr = N / r;
+  const size_t vb = round_up((size_t)((int64_t)r * B * H * ((Nr + 3) / 4 * 4)) * 4);
+  BwdWorkspace w{};
+  size_t off = 0;
+  w.xq = off; off += t;
+  w.xk = off; off += t;
+  w.xv = off; off += t;
+  w.xo = off; off += t;
+  w.xdo = off; off += t;
+  w.xl = off; off += lb;
+  w.xdq = off; off += t;
+  w.xdk = off; off += t;
+  w.xdv = off; off += t;
+  w.delta = off; off += vb;
+  w.l2 = off; off += vb;
+  w.total = off;
+  (void)u;
+  return w;
+}
+
 struct FwdWorkspace {
   size_t xq, xk, xv, parts_o, parts_l, xo, xl, total;
 };
@@ -342,6 +371,7 @@ int usp_lse_merge(const void* outs, const float* lses, int R, void* out, float* 
 size_t usp_attention_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring,
                                      usp_dtype dtype, usp_mode mode, int backward) {
   if (check_dims(B, H, N, D, ulysses, ring) != USP_OK || check_kernel(dtype, D) != USP_OK) return 0;
+  if (backward && mode == USP_MATERIALISED) return bwd_layout(B, H, N, D, ulysses, ring, dtype).total;
   if (backward) return 2 * bwd_vec_bytes(B, H, N, ulysses, ring);  // Delta and lse*log2(e)
   if (mode == USP_FUSED) return 0;
   return fwd_layout(B, H, N, D, ring, dtype).total;
@@ -654,7 +684,7 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
   cudaError_t e;
   if (dtype == USP_F32) {
     e = launch_attn_f32_bwd((const float*)q, (const float*)k, (const float*)v, (const float*)out, lse,
-                            (const float*)dout, (float*)dq, (float*)dk, (float*)dv, delta, B * H, sp, Ns, (int)D,
+                            (const float*)dout, (float*)dq, (float*)dk, (float*)dv, delta, B * H, sp, Ns, 1, (int)D,
                             scale, s);
   } else {
     Guard g;
@@ -664,12 +694,80 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
     a.q = q; a.k = k; a.v = v; a.out = out; a.dout = dout; a.lse = lse;
     a.dq = dq; a.dk = dk; a.dv = dv;
     a.delta = delta; a.l2 = l2;
-    a.BH = B * H; a.sp = sp; a.Ns = Ns;
+    a.BH = B * H; a.sp = sp; a.Ns = Ns; a.useg = 1;
     a.scale = scale;
     phase_begin(s);
     e = launch_attn_tc_bwd(a, g, s);  // marks a phase after each of its three kernels
   }
   return e == cudaSuccess ? USP_OK : cuda_fail(e);
+}
+
+int usp_attention_bwd_materialised(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                                   const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
+                                   int64_t D, int ulysses, int ring, float scale, usp_dtype dtype, void* workspace,
+                                   size_t workspace_bytes, usp_stream_t stream) {
+  int st = check_dims(B, H, N, D, ulysses, ring);
+  if (st != USP_OK) return st;
+  if (!std::isfinite(scale)) return USP_ERR_INVALID_ARG;
+  st = check_kernel(dtype, D);
+  if (st != USP_OK) return st;
+  if (B * H * N == 0) return USP_OK;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return USP_ERR_INVALID_ARG;
+  if (dtype == USP_BF16 && !(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(out, 16) &&
+                             aligned(dout, 16) && aligned(dq, 16) && aligned(dk, 16) && aligned(dv, 16)))
+    return USP_ERR_INVALID_ARG;
+  if (!aligned(lse, 4)) return USP_ERR_INVALID_ARG;
+  const int u = ulysses, r = ring;
+  const BwdWorkspace w = bwd_layout(B, H, N, D, u, r, dtype);
+  if (!workspace || workspace_bytes < w.total) return USP_ERR_WORKSPACE;
+  if (!aligned(workspace, 256)) return USP_ERR_INVALID_ARG;
+  const int64_t sp = (int64_t)u * r, Ns = N / sp, Nr = N / r, Hu = H / u;
+  if (B * H > 65535 || (Nr + 127) / 128 * r > 2147483647LL) return USP_ERR_UNSUPPORTED;
+  char* ws = static_cast<char*>(workspace);
+  const int elt = (int)elt_size(dtype);
+  cudaStream_t s = (cudaStream_t)stream;
+  Guard g;
+  if (dtype == USP_BF16 && (st = guard(&g)) != USP_OK) return st;
+  phase_begin(s);
+  {  // Ulysses token -> head of the five same-shape inputs in one launch, then the lse
+    const void* srcs[5] = {q, k, v, out, dout};
+    void* dsts[5] = {ws + w.xq, ws + w.xk, ws + w.xv, ws + w.xo, ws + w.xdo};
+    cudaError_t e = launch_relayout_n(srcs, dsts, 5, B, H, Ns, D, u, r, elt, true, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if ((st = relayout(lse, ws + w.xl, B, H, N, 1, u, r, 4, true, s)) != USP_OK) return st;
+  phase_mark(s);
+  // Every (ring rank g, Ulysses rank j) unit over all ring chunks of its
+  // heads, with the merged lse: the head-sharded stack viewed as
+  // [r*u][B*Hu][Nr][D], whose unit (j, b, h') owns the segments g*u + j.
+  float* delta = reinterpret_cast<float*>(ws + w.delta);
+  cudaError_t e;
+  if (dtype == USP_F32) {
+    e = launch_attn_f32_bwd((const float*)(ws + w.xq), (const float*)(ws + w.xk), (const float*)(ws + w.xv),
+                            (const float*)(ws + w.xo), (const float*)(ws + w.xl), (const float*)(ws + w.xdo),
+                            (float*)(ws + w.xdq), (float*)(ws + w.xdk), (float*)(ws + w.xdv), delta, B * Hu, sp, Nr,
+                            u, (int)D, scale, s);
+    if (e == cudaSuccess) phase_mark(s);
+  } else {
+    TcBwdArgs a{};
+    a.q = ws + w.xq; a.k = ws + w.xk; a.v = ws + w.xv; a.out = ws + w.xo; a.dout = ws + w.xdo;
+    a.lse = reinterpret_cast<const float*>(ws + w.xl);
+    a.dq = ws + w.xdq; a.dk = ws + w.xdk; a.dv = ws + w.xdv;
+    a.delta = delta; a.l2 = reinterpret_cast<float*>(ws + w.l2);
+    a.BH = B * Hu; a.sp = sp; a.Ns = Nr; a.useg = u;
+    a.scale = scale;
+    e = launch_attn_tc_bwd(a, g, s);  // marks a phase after each of its three kernels
+    if (e == cudaSuccess) phase_mark(s);  // both kernels joined back on `s`
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  {  // the gradients head -> token in one launch
+    const void* srcs[3] = {ws + w.xdq, ws + w.xdk, ws + w.xdv};
+    void* dsts[3] = {dq, dk, dv};
+    e = launch_relayout_n(srcs, dsts, 3, B, H, Ns, D, u, r, elt, false, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  phase_mark(s);
+  return USP_OK;
 }
 
 int usp_device_status(usp_stream_t stream) {

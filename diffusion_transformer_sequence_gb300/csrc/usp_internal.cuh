@@ -38,7 +38,7 @@ cudaError_t launch_relayout(const void* src, void* dst, int64_t runs_outer, int6
                             int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                             cudaStream_t stream);
 
-// The same re-layout of up to three same-shape tensors in one launch.
+// The same re-layout of up to five same-shape tensors in one launch.
 cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
                               int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                               cudaStream_t stream);
@@ -150,21 +150,26 @@ cudaError_t launch_attn_fp8_fwd(const Fp8AttnArgs& a, const Guard& g, cudaStream
 
 // bf16 tcgen05 backward over token-sharded stacks (D = 128): prep (Delta,
 // lse*log2e into workspace), dK/dV kernel, dQ kernel.
+// All tensors are stacks [sp][BH][Ns][D] (lse, delta, l2 without D): the
+// token-sharded stack (useg = 1: unit = head, over all sp segments) or the
+// head-sharded stack of the materialised path viewed as [r*u][B*Hu][Nr][D]
+// (useg = u: unit = (j, b, h'), over the segments g*u + j).
 struct TcBwdArgs {
   const void *q, *k, *v, *out, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  float* delta;  // workspace [sp][BH][Ns]
-  float* l2;     // workspace [sp][BH][Ns]
+  float* delta;  // workspace [sp][BH][Ns_pad]
+  float* l2;     // workspace [sp][BH][Ns_pad]
   int64_t BH, sp, Ns;
+  int useg;
   float scale;
 };
 cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t stream);
 
-// fp32 backward on the FP32 pipes over token-sharded stacks.
+// fp32 backward on the FP32 pipes over stacks (segment stride useg as in TcBwdArgs).
 cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, const float* out,
                                 const float* lse, const float* dout, float* dq, float* dk, float* dv,
-                                float* delta, int64_t BH, int64_t sp, int64_t Ns, int D, float scale,
+                                float* delta, int64_t BH, int64_t sp, int64_t Ns, int useg, int D, float scale,
                                 cudaStream_t stream);
 
 // Records the next phase event of the current call on stream `s` (no-op

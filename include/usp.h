@@ -120,9 +120,11 @@ int usp_attn_chunk_fwd(const void* q, const void* k, const void* v, void* out, f
 int usp_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
                   int64_t B, int64_t H, int64_t Nq, int64_t D, usp_dtype dtype, usp_stream_t stream);
 
-/* Bytes of workspace usp_attention_fwd (backward = 0) or usp_attention_bwd
- * (backward = 1) needs for this problem; 0 when none is needed.  Returns 0
- * as well for arguments the call itself would reject. */
+/* Bytes of workspace usp_attention_fwd (backward = 0) or the backward
+ * (backward = 1: usp_attention_bwd with USP_FUSED, usp_attention_bwd_materialised
+ * with USP_MATERIALISED, which also covers usp_attention_bwd) needs for this
+ * problem; 0 when none is needed.  Returns 0 as well for arguments the call
+ * itself would reject. */
 size_t usp_attention_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring,
                                      usp_dtype dtype, usp_mode mode, int backward);
 
@@ -160,6 +162,26 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
                       const void* dout, void* dq, void* dk, void* dv, int64_t B, int64_t H, int64_t N,
                       int64_t D, int ulysses, int ring, float scale, usp_dtype dtype, void* workspace,
                       size_t workspace_bytes, usp_stream_t stream);
+
+/* The same backward through the materialised Ulysses path ([PR] Numerics:
+ * the all-to-all is a permutation, so the gradients pass through its
+ * inverse; each ring step uses its own KV chunk and the merged lse):
+ *   tok2head(q, k, v, O, dO) in one launch and tok2head(lse) ->
+ *   per (ring rank g, Ulysses rank j, ring step t) the chunk backward of
+ *   query chunk g against KV chunk (g - t) mod ring over the head-sharded
+ *   stacks, dQ summed over t and dK/dV summed over the query chunks ->
+ *   head2tok(dq, dk, dv) in one launch.
+ * Same arguments, layouts and results as usp_attention_bwd (the sums run
+ * in another order, so results agree to rounding, not bit for bit).
+ * Needs usp_attention_workspace_bytes(..., USP_MATERIALISED, 1): eight
+ * head-sharded tensors plus the lse and two per-row vectors.  The bf16 path
+ * forks its dQ kernel as usp_attention_bwd does.
+ * Errors: as usp_attention_bwd. */
+int usp_attention_bwd_materialised(const void* q, const void* k, const void* v, const void* out,
+                                   const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                                   int64_t B, int64_t H, int64_t N, int64_t D, int ulysses, int ring,
+                                   float scale, usp_dtype dtype, void* workspace, size_t workspace_bytes,
+                                   usp_stream_t stream);
 
 /* Bytes of workspace usp_attention_fwd_joint needs (0 for USP_FUSED);
  * with_text_queries = 1 when q_txt will be given.  Returns 0 as well for
@@ -266,12 +288,16 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
  *                         (the two kernels run concurrently; both phases
  *                         are timed from the end of the prep)
+ *   bf16 materialised backward: [tok2head q,k,v,O,dO and lse] [prep]
+ *                         [dK,dV kernel] [dQ kernel] [join: end of dQ to
+ *                         the end of both] [head2tok dq,dk,dv]
  *   FP8 forward:          [quantise q, k, v] [FP8 attention]
  *   joint fused:          [attention: image and text queries, one launch]
  *   joint materialised:   [tok2head q,k,v] [partials against the image chunks
  *                         and against the text] [merge] [head2tok x2]
  *                         [text-query merge]
- * (the fp32 paths record nothing).  The events
+ * (the fp32 fused forward and usp_attention_bwd record nothing; the fp32
+ * materialised backward records [tok2head] [backward] [head2tok]).  The events
  * are created by the library on first enable.  Returns USP_OK or USP_ERR_CUDA. */
 int usp_profile_phases(int enable);
 

@@ -95,6 +95,33 @@ def test_attention_validation_and_workspace(L):
     assert f(None, None, None, None, None, 1, 8, 0, 32, 4, 1, 0.1, 0, 1, None, 0, None) == 0  # empty
 
 
+def test_backward_validation_and_workspace(L):
+    a = (FAKE,) * 5 + (FAKE,) * 4
+    for f in (L.usp_attention_bwd, L.usp_attention_bwd_materialised):
+        assert f(*a, 1, 40, 32768, 128, 16, 1, 0.1, 1, None, 0, None) == 2   # ulysses > H (40 % 16)
+        assert f(*a, 1, 40, 32770, 128, 8, 4, 0.1, 1, None, 0, None) == 2    # N % sp
+        assert f(*a, 1, 40, 32768, 64, 8, 4, 0.1, 1, None, 0, None) == 3     # bf16 D != 128
+        assert f(*a, 1, 40, 32768, 128, 8, 4, float("nan"), 1, None, 0, None) == 1
+        assert f(*a, 1, 40, 32768, 128, 8, 4, 0.1, 1, None, 0, None) == 4    # no workspace
+        assert f(*((None,) * 9), 1, 8, 0, 32, 4, 1, 0.1, 0, None, 0, None) == 0  # empty
+    # fused: Delta and lse*log2(e), rows of each (rank, head) padded to 4
+    fused = L.usp_attention_workspace_bytes(1, 40, 32768, 128, 8, 4, 1, 1, 1)
+    assert fused == 2 * 32 * 40 * 1024 * 4
+    # materialised: q, k, v, O, dO, dq, dk, dv head-sharded, the lse, and the
+    # two vectors over [ring * ulysses][B * Hu][Nr]
+    mat = L.usp_attention_workspace_bytes(1, 40, 32768, 128, 8, 4, 1, 0, 1)
+    t = 40 * 32768 * 128 * 2
+    assert mat == 8 * t + 40 * 32768 * 4 + 2 * 4 * 40 * 8192 * 4
+    assert L.usp_attention_bwd_materialised(*a, 1, 40, 32768, 128, 8, 4, 0.1, 1, FAKE, mat - 1, None) == 4
+    # Nr = 75600 / 2 = 37800 rows per ring chunk (a multiple of 4 already)
+    assert L.usp_attention_workspace_bytes(1, 40, 75600, 128, 8, 2, 1, 0, 1) == \
+        8 * 40 * 75600 * 128 * 2 + 40 * 75600 * 4 + 2 * 2 * 40 * 37800 * 4
+    # ragged: Nr = 6 rows pad to 8, every buffer rounded to 256 bytes
+    got = L.usp_attention_workspace_bytes(1, 4, 12, 32, 2, 2, 0, 0, 1)
+    rnd = lambda x: (x + 255) // 256 * 256
+    assert got == 8 * rnd(4 * 12 * 32 * 4) + rnd(4 * 12 * 4) + 2 * rnd(2 * 4 * 8 * 4)
+
+
 def test_joint_validation_and_workspace(L):
     f = L.usp_attention_fwd_joint
     img = (FAKE, FAKE, FAKE)

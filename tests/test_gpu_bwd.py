@@ -1,4 +1,5 @@
-"""GPU parity of usp_attention_bwd against the oracle, through the C ABI.
+"""GPU parity of usp_attention_bwd and usp_attention_bwd_materialised against
+the oracle, through the C ABI.
 
 Small problems: every row of dq, dk, dv against oracle.attention_bwd, with the
 backward fed the oracle's own forward (out rounded to the input dtype, lse to
@@ -53,8 +54,9 @@ SMALL = [
 ]
 
 
+@pytest.mark.parametrize("mode", ["fused", "materialised"])
 @pytest.mark.parametrize("dtype,B,H,N,u,r", SMALL)
-def test_bwd_small_full_rows(dtype, B, H, N, u, r):
+def test_bwd_small_full_rows(dtype, B, H, N, u, r, mode):
     usp = _usp()
     D = 128 if dtype == "bf16" else 32
     w = wl.custom("bwd", dtype, B, H, N, D, u, r, seed=N + 7 * H, backward=True)
@@ -69,18 +71,19 @@ def test_bwd_small_full_rows(dtype, B, H, N, u, r):
     dq, dk, dv = (c.view for c in cans)
     L = usp.lib()
     from diffusion_transformer_sequence_gb300 import _lib
-    need = usp.workspace_bytes(B, H, N, D, u, r, w.torch_dtype, backward=True)
+    need = usp.workspace_bytes(B, H, N, D, u, r, w.torch_dtype, mode=mode, backward=True)
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     args = [st(q), st(k), st(v), st(o_in), st(l_in), st(do)]
-    rc = L.usp_attention_bwd(*[a.data_ptr() for a in args], dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
-                             u, r, w.scale, _lib.USP_F32 if dtype == "f32" else _lib.USP_BF16, ws.data_ptr(), need,
-                             torch.cuda.current_stream().cuda_stream)
+    fn = L.usp_attention_bwd if mode == "fused" else L.usp_attention_bwd_materialised
+    rc = fn(*[a.data_ptr() for a in args], dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+            u, r, w.scale, _lib.USP_F32 if dtype == "f32" else _lib.USP_BF16, ws.data_ptr(), need,
+            torch.cuda.current_stream().cuda_stream)
     assert rc == 0
     assert usp.device_status() == 0
     for c in cans:
         c.check()
     for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
-        _check_grad(wl.from_token_stack(got.cpu()), ref, dtype, f"{name} {dtype} B{B} H{H} N{N} u{u} r{r}")
+        _check_grad(wl.from_token_stack(got.cpu()), ref, dtype, f"{name} {mode} {dtype} B{B} H{H} N{N} u{u} r{r}")
 
 
 def test_bwd_wan_shapes_sampled():
@@ -95,6 +98,14 @@ def test_bwd_wan_shapes_sampled():
     dq2, dk2, dv2 = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], w.ulysses, w.ring, w.scale)
     for a, b in ((dq, dq2), (dk, dk2), (dv, dv2)):    # deterministic: no atomics anywhere
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # The materialised path re-lays the same tokens out head-sharded; with
+    # Ns = 1024 a multiple of the 128-row tile, every tile and every sum runs
+    # in the same order, so its gradients equal the fused ones bit for bit.
+    mq, mk, mv = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], w.ulysses, w.ring, w.scale,
+                                   mode="materialised")
+    assert usp.device_status() == 0
+    for name, a, b in (("dq", dq, mq), ("dk", dk, mk), ("dv", dv, mv)):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), f"materialised {name} differs from fused"
     heads = [0, 4, 5, 39]   # Hu = 5: heads 4 | 5 sit on either side of a Ulysses group boundary
     qrows = wl.sample_rows(w, 4096)
     g = torch.Generator().manual_seed(w.row_seed + 1)
