@@ -16,16 +16,6 @@
 namespace usp {
 namespace {
 
-__device__ __forceinline__ void load8(const __nv_bfloat16* p, float* f) {
-  uint4 raw = __ldg(reinterpret_cast<const uint4*>(p));
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
-  }
-}
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* f) {
   uint4 raw;
   __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&raw);
@@ -33,37 +23,43 @@ __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* f) {
   for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
   *reinterpret_cast<uint4*>(p) = raw;
 }
-__device__ __forceinline__ void load8(const float* p, float* f) {
-  float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
 __device__ __forceinline__ void store8(float* p, const float* f) {
   reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
   reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
 }
+// Eight elements held as loaded (packed bf16 stays 4 registers).
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint4*>(p)); }
+  __device__ __forceinline__ void get(float* f) const {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float* p) {
+    a = __ldg(reinterpret_cast<const float4*>(p));
+    b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  }
+  __device__ __forceinline__ void get(float* f) const {
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+  }
+};
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
 __device__ __forceinline__ void from_f(float* p, float x) { *p = x; }
 __device__ __forceinline__ void from_f(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
-
-// Row statistics: returns L, fills w[t] = exp(lse_t - L).  Computed with the
-// hardware exp2 / log2 approximations (relative error ~1e-7, far inside the
-// merge's fp32 and bf16 tolerances) to keep the kernel memory-bound.
-template <int kMaxR>
-__device__ __forceinline__ float merge_weights(const float* __restrict__ lses, int R, int64_t rows,
-                                               int64_t row, float* w) {
-  float m = -INFINITY;
-  for (int t = 0; t < R; ++t) m = fmaxf(m, __ldg(lses + t * rows + row));
-  float s = 0.f;
-  for (int t = 0; t < R; ++t) s += __expf(__ldg(lses + t * rows + row) - m);
-  const float L = m + __logf(s);
-#pragma unroll
-  for (int t = 0; t < kMaxR; ++t)
-    if (t < R) w[t] = __expf(__ldg(lses + t * rows + row) - L);
-  return L;
-}
 
 // 8 elements (16 or 32 bytes) per thread; D % 8 == 0, R <= kMaxR.
 template <typename T, int kMaxR>
@@ -76,19 +72,40 @@ __global__ void __launch_bounds__(256) merge_vec_kernel(const T* __restrict__ ou
   const int64_t row = gt / tpr;
   const int64_t c = (gt - row * tpr) * 8;
   if (row >= rows) return;
-  float w[kMaxR];
-  const float L = merge_weights<kMaxR>(lses, R, rows, row, w);
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  // every load of the thread is issued before any arithmetic (the partials
+  // and the LSEs are independent, so their memory latencies overlap); the
+  // row statistics use the hardware exp2 / log2 approximations (relative
+  // error ~1e-7, far inside the merge's fp32 and bf16 tolerances)
   const int64_t plane = rows * D;
+  Raw8<T> x[kMaxR];
+  float lv[kMaxR];
 #pragma unroll
   for (int t = 0; t < kMaxR; ++t) {
     if (t < R) {
-      float x[8];
-      load8(outs + t * plane + row * D + c, x);
+      x[t].load(outs + t * plane + row * D + c);
+      lv[t] = __ldg(lses + t * rows + row);
+    }
+  }
+  float m = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(w[t], x[i], acc[i]);
+  for (int t = 0; t < kMaxR; ++t)
+    if (t < R) m = fmaxf(m, lv[t]);
+  float s = 0.f;
+#pragma unroll
+  for (int t = 0; t < kMaxR; ++t)
+    if (t < R) s += __expf(lv[t] - m);
+  const float L = m + __logf(s);
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+  for (int t = 0; t < kMaxR; ++t) {
+    if (t < R) {
+      const float wt = __expf(lv[t] - L);
+      float f[8];
+      x[t].get(f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt, f[i], acc[i]);
     }
   }
   store8(out + row * D + c, acc);

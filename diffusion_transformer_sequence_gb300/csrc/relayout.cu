@@ -22,18 +22,22 @@ constexpr int kUnroll = 4;
 template <typename Vec>
 __device__ __forceinline__ Vec load_stream(const Vec* p) { return __ldg(p); }
 
-// Up to five tensors of the same shape per launch (blockIdx.z picks one):
-// q, k and v of the materialised forward (and q, k, v, O, dO of the
-// materialised backward) go through one launch.
-constexpr int kMaxTensors = 5;
+// Up to six tensors per launch (blockIdx.z picks one), with the same run
+// layout but each its own run length: q, k and v of the materialised forward
+// (q, k, v, O, dO and the LSE of the materialised backward) go through one
+// launch, and so do an output and its LSE.
+constexpr int kMaxTensors = 6;
 struct Tensors {
   const void* src[kMaxTensors];
   void* dst[kMaxTensors];
+  int64_t run_vecs[kMaxTensors];
 };
 
 template <typename Vec, bool kTok2Head>
-__global__ void __launch_bounds__(kThreads) relayout_kernel(Tensors ts, int64_t nruns, int64_t run_vecs,
+__global__ void __launch_bounds__(kThreads) relayout_kernel(const __grid_constant__ Tensors ts, int64_t nruns,
                                                             int64_t B, int64_t H, int64_t Hu, int64_t u) {
+  const int64_t run_vecs = ts.run_vecs[blockIdx.z];
+  if ((int64_t)blockIdx.x * kThreads * kUnroll >= run_vecs) return;  // a shorter tensor of the launch
   const Vec* __restrict__ src = static_cast<const Vec*>(ts.src[blockIdx.z]);
   Vec* __restrict__ dst = static_cast<Vec*>(ts.dst[blockIdx.z]);
   for (int64_t run = blockIdx.y; run < nruns; run += gridDim.y) {
@@ -77,43 +81,57 @@ __global__ void __launch_bounds__(kThreads) relayout_kernel(Tensors ts, int64_t 
 }
 
 template <typename Vec>
-cudaError_t launch_vec(const Tensors& ts, int count, int64_t nruns, int64_t run_bytes, int64_t B, int64_t H,
+cudaError_t launch_vec(Tensors ts, int count, int64_t nruns, const int64_t* run_bytes, int64_t B, int64_t H,
                        int64_t Hu, int64_t u, bool tok2head, cudaStream_t stream) {
-  const int64_t run_vecs = run_bytes / (int64_t)sizeof(Vec);
+  int64_t run_vecs = 0;  // longest run of the launch, in vectors
+  for (int i = 0; i < count; ++i) {
+    ts.run_vecs[i] = run_bytes[i] / (int64_t)sizeof(Vec);
+    if (ts.run_vecs[i] > run_vecs) run_vecs = ts.run_vecs[i];
+  }
   const int64_t per_cta = (int64_t)kThreads * kUnroll;
   int64_t gx = (run_vecs + per_cta - 1) / per_cta;
   if (gx > 1024) gx = 1024;
   int64_t gy = nruns < 65535 ? nruns : 65535;
   dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)count);
   if (tok2head)
-    relayout_kernel<Vec, true><<<grid, kThreads, 0, stream>>>(ts, nruns, run_vecs, B, H, Hu, u);
+    relayout_kernel<Vec, true><<<grid, kThreads, 0, stream>>>(ts, nruns, B, H, Hu, u);
   else
-    relayout_kernel<Vec, false><<<grid, kThreads, 0, stream>>>(ts, nruns, run_vecs, B, H, Hu, u);
+    relayout_kernel<Vec, false><<<grid, kThreads, 0, stream>>>(ts, nruns, B, H, Hu, u);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
-                              int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
-                              cudaStream_t stream) {
+cudaError_t launch_relayout_rows(const void* const* srcs, void* const* dsts, const int64_t* row_bytes, int count,
+                                 int64_t B, int64_t H, int64_t Ns, int ulysses, int ring, bool tok2head,
+                                 cudaStream_t stream) {
   if (count < 1 || count > kMaxTensors) return cudaErrorInvalidValue;
   const int64_t u = ulysses;
   const int64_t Hu = H / u;
   const int64_t nruns = (int64_t)ring * u * B * H;
-  const int64_t run_bytes = Ns * D * elt;
   Tensors ts{};
-  uintptr_t a = (uintptr_t)run_bytes;
+  int64_t run_bytes[kMaxTensors];
+  uintptr_t a = 0;
   for (int i = 0; i < count; ++i) {
     ts.src[i] = srcs[i];
     ts.dst[i] = dsts[i];
-    a |= (uintptr_t)srcs[i] | (uintptr_t)dsts[i];
+    run_bytes[i] = Ns * row_bytes[i];
+    a |= (uintptr_t)srcs[i] | (uintptr_t)dsts[i] | (uintptr_t)run_bytes[i];
   }
   if ((a & 15) == 0) return launch_vec<uint4>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
   if ((a & 7) == 0) return launch_vec<uint2>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
   if ((a & 3) == 0) return launch_vec<uint32_t>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
   if ((a & 1) == 0) return launch_vec<uint16_t>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
   return launch_vec<uint8_t>(ts, count, nruns, run_bytes, B, H, Hu, u, tok2head, stream);
+}
+
+cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
+                              int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
+                              cudaStream_t stream) {
+  if (count < 1 || count > kMaxTensors) return cudaErrorInvalidValue;
+  int64_t rb[kMaxTensors];
+  for (int i = 0; i < count; ++i) rb[i] = D * elt;
+  return launch_relayout_rows(srcs, dsts, rb, count, B, H, Ns, ulysses, ring, tok2head, stream);
 }
 
 cudaError_t launch_relayout(const void* src, void* dst, int64_t /*runs_outer*/, int64_t B, int64_t H,

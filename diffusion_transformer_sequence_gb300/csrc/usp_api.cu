@@ -211,6 +211,26 @@ int relayout(const void* src, void* dst, int64_t B, int64_t H, int64_t N, int64_
   return e == cudaSuccess ? USP_OK : cuda_fail(e);
 }
 
+// A stack of rows of D elements and its fp32 LSE stack, re-laid out the same
+// way: one launch when both move in 16-byte vectors (Ns a multiple of 4),
+// else one launch each (the LSE's 4-byte runs would slow the big tensor).
+int relayout_with_lse(const void* x, void* x_dst, const float* l, float* l_dst, int64_t B, int64_t H, int64_t N,
+                      int64_t D, int u, int r, int elt, bool tok2head, cudaStream_t s) {
+  const int64_t Ns = N / ((int64_t)u * r);
+  const uintptr_t a = (uintptr_t)x | (uintptr_t)x_dst | (uintptr_t)l | (uintptr_t)l_dst |
+                      (uintptr_t)(Ns * 4) | (uintptr_t)(Ns * D * elt);
+  if ((a & 15) == 0) {
+    const void* srcs[2] = {x, l};
+    void* dsts[2] = {x_dst, l_dst};
+    const int64_t rb[2] = {D * elt, 4};
+    cudaError_t e = launch_relayout_rows(srcs, dsts, rb, 2, B, H, Ns, u, r, tok2head, s);
+    return e == cudaSuccess ? USP_OK : cuda_fail(e);
+  }
+  int st = relayout(x, x_dst, B, H, N, D, u, r, elt, tok2head, s);
+  if (st != USP_OK) return st;
+  return relayout(l, l_dst, B, H, N, 1, u, r, 4, tok2head, s);
+}
+
 // Attention of one or two problems on the kernel for `dt`: bf16 runs both
 // in one tcgen05 launch, fp32 (FP32 pipes) one launch per problem.
 int run_attention(const AttnArgs* a, int n, usp_dtype dt, int64_t D, cudaStream_t s) {
@@ -429,8 +449,7 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
     if (e != cudaSuccess) return cuda_fail(e);
   }
   phase_mark(s);
-  if ((st = relayout(ws + w.xo, out, B, H, N, D, u, r, elt, false, s)) != USP_OK) return st;
-  st = relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s);
+  st = relayout_with_lse(ws + w.xo, out, (const float*)(ws + w.xl), lse, B, H, N, D, u, r, elt, false, s);
   phase_mark(s);
   return st;
 }
@@ -561,8 +580,9 @@ int usp_attention_fwd_joint(const void* q, const void* k, const void* v, const v
                                      (float*)(ws + w.xl), BH * N, D, (int)dtype, s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (prof) phase_mark(s);
-    if ((st = relayout(ws + w.xo, out, B, H, N, D, u, r, elt, false, s)) != USP_OK) return st;
-    if ((st = relayout(ws + w.xl, lse, B, H, N, 1, u, r, 4, false, s)) != USP_OK) return st;
+    if ((st = relayout_with_lse(ws + w.xo, out, (const float*)(ws + w.xl), lse, B, H, N, D, u, r, elt, false, s)) !=
+        USP_OK)
+      return st;
     if (prof) phase_mark(s);
   }
   if (tq) {
@@ -729,13 +749,16 @@ int usp_attention_bwd_materialised(const void* q, const void* k, const void* v, 
   Guard g;
   if (dtype == USP_BF16 && (st = guard(&g)) != USP_OK) return st;
   phase_begin(s);
-  {  // Ulysses token -> head of the five same-shape inputs in one launch, then the lse
-    const void* srcs[5] = {q, k, v, out, dout};
-    void* dsts[5] = {ws + w.xq, ws + w.xk, ws + w.xv, ws + w.xo, ws + w.xdo};
-    cudaError_t e = launch_relayout_n(srcs, dsts, 5, B, H, Ns, D, u, r, elt, true, s);
+  {  // Ulysses token -> head of q, k, v, O, dO and the lse: one launch when the
+     // lse runs are 16-byte multiples (Ns % 4 == 0), else the lse separately
+    const void* srcs[6] = {q, k, v, out, dout, lse};
+    void* dsts[6] = {ws + w.xq, ws + w.xk, ws + w.xv, ws + w.xo, ws + w.xdo, ws + w.xl};
+    const int64_t rb[6] = {D * elt, D * elt, D * elt, D * elt, D * elt, 4};
+    const bool with_lse = ((Ns * 4) & 15) == 0 && aligned(lse, 16);
+    cudaError_t e = launch_relayout_rows(srcs, dsts, rb, with_lse ? 6 : 5, B, H, Ns, u, r, true, s);
     if (e != cudaSuccess) return cuda_fail(e);
+    if (!with_lse && (st = relayout(lse, ws + w.xl, B, H, N, 1, u, r, 4, true, s)) != USP_OK) return st;
   }
-  if ((st = relayout(lse, ws + w.xl, B, H, N, 1, u, r, 4, true, s)) != USP_OK) return st;
   phase_mark(s);
   // Every (ring rank g, Ulysses rank j) unit over all ring chunks of its
   // heads, with the merged lse: the head-sharded stack viewed as

@@ -38,7 +38,13 @@ cudaError_t launch_relayout(const void* src, void* dst, int64_t runs_outer, int6
                             int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                             cudaStream_t stream);
 
-// The same re-layout of up to five same-shape tensors in one launch.
+// The same re-layout of up to six tensors in one launch whose rows are
+// row_bytes[i] bytes (D * element size); run alignment picks the vector width
+// for the whole launch.
+cudaError_t launch_relayout_rows(const void* const* srcs, void* const* dsts, const int64_t* row_bytes, int count,
+                                 int64_t B, int64_t H, int64_t Ns, int ulysses, int ring, bool tok2head,
+                                 cudaStream_t stream);
+// The same re-layout of up to six same-shape tensors in one launch.
 cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int count, int64_t B, int64_t H,
                               int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                               cudaStream_t stream);

@@ -284,7 +284,8 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  * usp_attention_fwd / usp_attention_bwd call on this thread records a CUDA
  * event on its stream before its first kernel and after each kernel group:
  *   fused forward:        [attention]
- *   materialised forward: [tok2head q,k,v] [chunk attention] [merge] [head2tok x2]
+ *   materialised forward: [tok2head q,k,v] [chunk attention] [merge]
+ *                         [head2tok of out and lse (one launch when Ns % 4 == 0)]
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
  *                         (the two kernels run concurrently; both phases
  *                         are timed from the end of the prep)
@@ -294,7 +295,7 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *   FP8 forward:          [quantise q, k, v] [FP8 attention]
  *   joint fused:          [attention: image and text queries, one launch]
  *   joint materialised:   [tok2head q,k,v] [partials against the image chunks
- *                         and against the text] [merge] [head2tok x2]
+ *                         and against the text] [merge] [head2tok of out and lse]
  *                         [text-query merge]
  * (the fp32 fused forward and usp_attention_bwd record nothing; the fp32
  * materialised backward records [tok2head] [backward] [head2tok]).  The events
