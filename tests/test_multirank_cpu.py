@@ -66,3 +66,15 @@ def test_two_rank_gloo_host_logic():
     assert w0 == w1 == 0.020                       # max over ranks, identical on both
     assert abs(v0 - 2 * 1e12 / 0.020 / 1e12) < 1e-9 and v0 == v1
     assert '"impl": "reference"' in o0 and o1 == ""  # rank 0 alone prints
+    import json
+    lines = [l for l in o0.splitlines() if l.startswith("{")]
+    assert len(lines) == 1                           # one JSON line
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "t"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
