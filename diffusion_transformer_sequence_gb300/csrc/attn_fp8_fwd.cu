@@ -388,12 +388,9 @@ bool make_map_u8(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, 
 }  // namespace
 
 cudaError_t launch_attn_fp8_fwd(const Fp8AttnArgs& a, const Guard& g, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  const cudaError_t ea = smem_limit_once(attr, (const void*)attn_fp8_fwd_kernel, SMEM_BYTES);
+  if (ea != cudaSuccess) return ea;
   CUtensorMap mq, mk, mvt;
   if (!make_map_u8(&mq, a.q8, HD, a.Ns, a.BH, a.sp) || !make_map_u8(&mk, a.k8, HD, a.Ns, a.BH, a.sp) ||
       !make_map_u8(&mvt, a.vt8, a.Ns_pad, HD, a.BH, a.sp))

@@ -677,14 +677,10 @@ bool map_stack_f32(CUtensorMap* m, const void* base, int64_t Ns, int64_t Ns_pad,
 }  // namespace
 
 cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(usp_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(usp_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DQ_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr0{0}, attr1{0};
+  cudaError_t ea = smem_limit_once(attr0, (const void*)usp_bwd_dkdv_kernel, SMEM_BYTES);
+  if (ea == cudaSuccess) ea = smem_limit_once(attr1, (const void*)usp_bwd_dq_kernel, DQ_SMEM_BYTES);
+  if (ea != cudaSuccess) return ea;
   const int64_t rows = a.BH * a.sp * a.Ns;
   const int64_t Ns_pad = (a.Ns + 3) / 4 * 4;
   usp_bwd_prep_kernel<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, stream>>>(

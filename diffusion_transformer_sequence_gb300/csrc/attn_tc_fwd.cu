@@ -563,15 +563,10 @@ bool make_kv(const AttnArgs& a, TcParams* p, KvMaps* m) {
 }  // namespace
 
 cudaError_t launch_attn_tc_fwd(const AttnArgs* sides, int nsides, const Guard& g, cudaStream_t stream) {
-  static bool attr_set = false;  // per process; the attribute is per function, not per device
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_BYTES);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(attn_tc_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr0{0}, attr1{0};
+  cudaError_t ea = smem_limit_once(attr0, (const void*)attn_tc_fwd_kernel<false>, SMEM_BYTES);
+  if (ea == cudaSuccess) ea = smem_limit_once(attr1, (const void*)attn_tc_fwd_kernel<true>, SMEM_BYTES);
+  if (ea != cudaSuccess) return ea;
   if (nsides < 1 || nsides > 2) return cudaErrorInvalidValue;
   const AttnArgs& a0 = sides[0];
   if (nsides == 2) {  // the two query sets share the KV sources, the stack geometry and the scale

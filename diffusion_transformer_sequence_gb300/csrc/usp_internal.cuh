@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace usp {
 
 // Error codes written into the per-device error word by kernels whose waits
@@ -15,6 +17,20 @@ enum DevError : unsigned int {
   kDevTimeoutSoftmax = 3,
   kDevTimeoutEpilogue = 4,
 };
+
+// Raises a kernel's dynamic shared-memory limit once per device (bit d of
+// `done` for device d < 64; devices beyond that set it on every launch).
+// Concurrent first calls may both set it, which is harmless.
+inline cudaError_t smem_limit_once(std::atomic<unsigned long long>& done, const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Per-launch guard: where to record an expired wait, and the wait limits.
 struct Guard {
