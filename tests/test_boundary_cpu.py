@@ -122,6 +122,22 @@ def test_backward_validation_and_workspace(L):
     assert got == 8 * rnd(4 * 12 * 32 * 4) + rnd(4 * 12 * 4) + 2 * rnd(2 * 4 * 8 * 4)
 
 
+def test_grid_limits(L):
+    """One past the largest launch grid (B*H = 65536 units) is rejected on the host."""
+    a = (FAKE,) * 5
+    assert L.usp_attention_fwd(*a, 2, 32768, 16, 128, 1, 1, 0.1, 1, 1, None, 0, None) == 3   # fused
+    ws = L.usp_attention_workspace_bytes(2, 32768, 16, 128, 1, 1, 1, 0, 0)
+    assert L.usp_attention_fwd(*a, 2, 32768, 16, 128, 1, 1, 0.1, 1, 0, FAKE, ws, None) == 3   # materialised
+    g = (FAKE,) * 9
+    ws = L.usp_attention_workspace_bytes(2, 32768, 16, 128, 1, 1, 1, 1, 1)
+    assert L.usp_attention_bwd(*g, 2, 32768, 16, 128, 1, 1, 0.1, 1, FAKE, ws, None) == 3
+    ws = L.usp_attention_workspace_bytes(2, 32768, 16, 128, 1, 1, 1, 0, 1)
+    assert L.usp_attention_bwd_materialised(*g, 2, 32768, 16, 128, 1, 1, 0.1, 1, FAKE, ws, None) == 3
+    # materialised forward: r*r*u*B*Hu units (here 2*2*1*B*H) past the grid
+    ws = L.usp_attention_workspace_bytes(1, 16384, 32, 128, 1, 2, 1, 0, 0)
+    assert L.usp_attention_fwd(*a, 1, 16384, 32, 128, 1, 2, 0.1, 1, 0, FAKE, ws, None) == 3
+
+
 def test_joint_validation_and_workspace(L):
     f = L.usp_attention_fwd_joint
     img = (FAKE, FAKE, FAKE)

@@ -1,0 +1,85 @@
+"""GPU parity at the edges of the supported envelope, through the C ABI.
+
+* The largest head count a launch grid takes: B*H = 65535 (u = r = 1, N = 8,
+  a single ragged 8-row tile per head) for the fused and materialised
+  forwards and both backward calls, every head against the oracle.
+* A 2^20-token sequence (B1 H2 D128, u2 x r4: 131072 tokens per virtual
+  rank), fused and materialised forward, on sampled rows (shard boundaries,
+  tile edges) of both heads against the oracle's unsharded attention.
+
+One past the grid limit (B*H = 65536) is rejected on the host; that case is
+in test_boundary_cpu.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from diffusion_transformer_sequence_gb300 import workloads as wl
+from tests.helpers import BF16_GRAD_REL, check_out, ensure_built, f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    ensure_built()
+    assert torch.cuda.is_available()
+
+
+def _usp():
+    import diffusion_transformer_sequence_gb300 as usp
+    return usp
+
+
+def _grad_ok(got, ref, what):
+    g = f64(got)
+    assert np.isfinite(g).all(), f"{what}: non-finite"
+    rel = np.abs(g - ref).max() / max(np.abs(ref).max(), 1e-30)
+    assert rel <= BF16_GRAD_REL, f"{what}: rel err {rel:.3e}"
+
+
+def test_max_heads_per_launch():
+    usp = _usp()
+    B, H, N, D = 5, 13107, 8, 128          # B*H = 65535 units: the largest grid the launches take
+    w = wl.custom("maxheads", "bf16", B, H, N, D, 1, 1, seed=65535, backward=True)
+    inp = wl.make_inputs(w)
+    q, k, v, do = (inp[n] for n in ("q", "k", "v", "dout"))
+    o_ref, l_ref = oracle.attention(f64(q), f64(k), f64(v), w.scale)
+    st = [wl.to_token_stack(t, 1, 1).cuda() for t in (q, k, v)]
+    for mode in ("fused", "materialised"):
+        o, l = usp.attention_fwd(*st, 1, 1, w.scale, mode=mode)
+        assert usp.device_status() == 0
+        check_out(wl.from_token_stack(o.cpu()), wl.from_token_stack(l.cpu()), o_ref, l_ref, "bf16",
+                  f"B*H=65535 {mode}")
+    # backward from the oracle's own forward, every head
+    dq_r, dk_r, dv_r = oracle.attention_bwd(f64(q), f64(k), f64(v), o_ref, l_ref, f64(do), w.scale)
+    o_in = wl.to_token_stack(torch.from_numpy(o_ref).to(torch.bfloat16), 1, 1).cuda()
+    l_in = wl.to_token_stack(torch.from_numpy(l_ref).float(), 1, 1).cuda()
+    do_d = wl.to_token_stack(do, 1, 1).cuda()
+    for mode in ("fused", "materialised"):
+        dq, dk, dv = usp.attention_bwd(*st, o_in, l_in, do_d, 1, 1, w.scale, mode=mode)
+        assert usp.device_status() == 0
+        for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+            _grad_ok(wl.from_token_stack(got.cpu()), ref, f"B*H=65535 {mode} {name}")
+
+
+def test_million_token_sequence():
+    usp = _usp()
+    u, r = 2, 4
+    w = wl.custom("n1m", "bf16", 1, 2, 1 << 20, 128, u, r, seed=1 << 20)
+    inp = wl.make_inputs(w, with_dout=False)
+    st = [wl.to_token_stack(inp[n], u, r).cuda() for n in ("q", "k", "v")]
+    rows = wl.sample_rows(w, 256)
+    flat = {n: inp[n].reshape(w.H, w.N, w.D).float().numpy() for n in ("q", "k", "v")}
+    ref = [oracle.attention_rows(flat["q"][h], flat["k"][h], flat["v"][h], rows.numpy(), w.scale, row_block=64)
+           for h in range(w.H)]
+    ro = np.stack([x[0] for x in ref])
+    rl = np.stack([x[1] for x in ref])
+    for mode in ("fused", "materialised"):
+        o, l = usp.attention_fwd(*st, u, r, w.scale, mode=mode)
+        assert usp.device_status() == 0
+        go = wl.from_token_stack(o).reshape(w.H, w.N, w.D)[:, rows.cuda()]
+        gl = wl.from_token_stack(l).reshape(w.H, w.N)[:, rows.cuda()]
+        check_out(go, gl, ro, rl, "bf16", f"N=2^20 {mode}")
+        del o, l
+        torch.cuda.empty_cache()
