@@ -34,9 +34,9 @@ Readings where the pages are silent or open:
 * The merge is the standard log-sum-exp combination (the pages name it but do
   not print it): m = max_t lse_t; L = m + ln sum_t exp(lse_t - m);
   O = sum_t exp(lse_t - L) O_t.
-* At ring step t, ring rank g holds KV chunk c = (g - t) mod ring
-  ("passed station by station"); the merged result does not depend on the
-  order up to rounding.
+* At ring step t, ring rank g holds KV chunk c = (g - t) mod ring (the
+  handbook's ring figure hands each K/V block on to the next rank once per
+  step); the merged result does not depend on the order up to rounding.
 * Virtual rank (g, j) has sp_rank = g * ulysses + j; its tokens are
   [sp_rank*Ns, (sp_rank+1)*Ns); Ulysses rank j owns heads
   [j*Hu, (j+1)*Hu); the head-sharded buffer concatenates the u source ranks
@@ -49,8 +49,8 @@ Readings where the pages are silent or open:
   ring chunk of their Ulysses head group.
 * Cross-attention: each rank's image queries attend to the replicated text
   K/V only; nothing is exchanged.
-* FP8 attention (the handbook's Wan table: "FP8 low precision" as the last
-  latency step; the pages print no scheme): q, k and v are quantised to
+* FP8 attention (the handbook's Wan latency table lists FP8 as its last
+  step; the pages print no scheme): q, k and v are quantised to
   OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
   infinities, largest finite 448, round to nearest even, saturating) with
   one scale per (b, h) head over the whole sequence, amax / 448; the
