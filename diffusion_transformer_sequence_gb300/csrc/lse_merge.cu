@@ -2,8 +2,8 @@
 //
 // "Multi-GPU parallelism: spreading one step over several cards", section
 // "Sequence parallelism: Ulysses and Ring": each KV block that arrives round
-// the ring yields a local attention result, and the results are merged with a
-// log-sum-exp (the online-softmax formula).  Per row, in fp32:
+// the ring yields a local attention result; a log-sum-exp merge (the
+// online-softmax rule) combines them.  Per row, in fp32:
 //   m = max_t lse_t;  L = m + ln sum_t exp(lse_t - m);  out = sum_t exp(lse_t - L) out_t
 // The merge is over the R ring steps of one row, not across D, so a row's D
 // elements are split over threads in 16-byte vectors and no cross-thread

@@ -1,8 +1,9 @@
 // libusp C ABI: argument validation, workspace layout and the USP drivers.
 //
-// The driver composes the steps of USP attention as the USP PR page's Design
-// describes usp_attention (Ulysses all-to-all, Ring steps with an
-// LSE-returning kernel, all-to-all back), with the virtual rank grid
+// The driver composes the steps of USP attention in the order the USP PR
+// page's Design gives them (the exchange within each Ulysses group, the ring
+// steps on a kernel that also yields the log-sum-exp, the exchange back),
+// with the virtual rank grid
 // ulysses x ring laid out on one device:
 //   * the all-to-all becomes the on-device re-layout (relayout.cu);
 //   * the ring's peer-to-peer KV rotation becomes addressing: at ring step t

@@ -144,8 +144,9 @@ def to_token_stack(x: torch.Tensor, ulysses: int, ring: int) -> torch.Tensor:
     """Place a global [B,H,N,D] (or [B,H,N]) tensor in the token-sharded stack.
 
     Virtual rank sp_rank takes the contiguous token slice
-    [sp_rank*Ns, (sp_rank+1)*Ns) of every head, exactly as the handbook's
-    simulation slices ``q[:, :, r*N//P:(r+1)*N//P]`` per card.  This is data
+    [sp_rank*Ns, (sp_rank+1)*Ns) of every head, the same token split as the
+    handbook's four-card simulation (card r takes the r-th of P equal token
+    segments).  This is data
     placement of the inputs, not a step of the method.
     """
     sp = ulysses * ring

@@ -7,12 +7,13 @@
  *  [HB] "Multi-GPU parallelism: spreading one step over several cards",
  *       section "Sequence parallelism: Ulysses and Ring": the Ulysses
  *       all-to-all (per-card token slices <-> per-card head groups), per-card
- *       attention, and the Ring step that merges per-KV-block results with a
- *       log-sum-exp (FlashAttention's online-softmax formula).
+ *       attention, and the Ring step that combines per-KV-block results by a
+ *       log-sum-exp merge (the online-softmax rule).
  *  [PR] "Feat: USP sequence parallelism (Ulysses x Ring) via
  *       SequenceParallelPlan; Wan enabled": Design ("Coordinates": sp =
  *       ulysses x ring, Ulysses ranks contiguous, ring ranks strided; "Ring
- *       kernel selection": kernels return LSE and pair with a real backward),
+ *       kernel selection": the ring kernels also produce the log-sum-exp and have
+ *       matching backward kernels),
  *       Limitations (the conditions that must fail loudly), Numerics.
  *  [VO] vllm-omni "Parallelism Acceleration Guide": sequence chunked by SP
  *       rank in rank order; hybrid sp = ulysses_degree x ring_degree.
@@ -145,9 +146,9 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
                       usp_dtype dtype, usp_mode mode, void* workspace, size_t workspace_bytes,
                       usp_stream_t stream);
 
-/* USP attention backward ([PR] Numerics: the all-to-all is a permutation so
- * gradients flow through its inverse; each ring step uses its own KV chunk
- * and the MERGED lse).  With P = exp(scale q k^T - lse):
+/* USP attention backward ([PR] Numerics: the Ulysses exchange only moves
+ * data, so the gradients take the inverse exchange; each ring step uses its
+ * own KV chunk and the MERGED lse).  With P = exp(scale q k^T - lse):
  *   dV = P^T dO, dP = dO V^T, Delta_i = sum_d dO_id O_id,
  *   dS = P * (dP - Delta), dQ = scale dS K, dK = scale dS^T Q.
  * q, k, v, out, dout, dq, dk, dv: token-sharded stacks in `dtype`; lse: the
@@ -164,8 +165,8 @@ int usp_attention_bwd(const void* q, const void* k, const void* v, const void* o
                       size_t workspace_bytes, usp_stream_t stream);
 
 /* The same backward through the materialised Ulysses path ([PR] Numerics:
- * the all-to-all is a permutation, so the gradients pass through its
- * inverse; each ring step uses its own KV chunk and the merged lse):
+ * the Ulysses exchange only moves data, so the gradients take the inverse
+ * exchange; each ring step uses its own KV chunk and the merged lse):
  *   tok2head(q, k, v, O, dO) in one launch and tok2head(lse) ->
  *   per (ring rank g, Ulysses rank j, ring step t) the chunk backward of
  *   query chunk g against KV chunk (g - t) mod ring over the head-sharded

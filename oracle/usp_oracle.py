@@ -11,14 +11,15 @@ Sources (page titles as extracted):
 * [HB]  "Multi-GPU parallelism: spreading one step over several cards",
   section "Sequence parallelism: Ulysses and Ring" -- the four-card Ulysses
   simulation (per-card token slices, ``all_to_all_heads``, per-card SDPA,
-  ``all_to_all_tokens``) and the statement that Ring merges the per-block
-  local results with a log-sum-exp, the formula of FlashAttention's online
-  softmax; the figure caption there: K and V blocks are "passed station by
-  station" around the ring.
+  ``all_to_all_tokens``) and its account of Ring: each K/V block handed
+  round the ring gives a local attention result, and a log-sum-exp merge
+  (the online-softmax rule) combines them; its ring figure moves every K/V
+  block on to the next rank once per step.
 * [PR]  "Feat: USP sequence parallelism (Ulysses x Ring) via
   SequenceParallelPlan; Wan enabled", Design, "Coordinates" (sp = ulysses x
   ring, Ulysses ranks contiguous, ring ranks strided), "Ring kernel
-  selection" (kernels return LSE and pair with a real backward), Numerics.
+  selection" (the ring kernels also produce the log-sum-exp and have
+  matching backward kernels), Numerics.
 * [VO]  vllm-omni "Parallelism Acceleration Guide", "How to parallelize a new
   model": tokens are chunked along the sequence by SP rank in rank order;
   Qwen-Image runs joint attention over concatenated text + image tokens and

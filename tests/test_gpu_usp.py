@@ -60,14 +60,14 @@ def test_page_demo_sharded_equals_unsharded():
     w = wl.WORKLOADS["demo"]
     inp = wl.make_inputs(w)
     st = [t.cuda() for t in _stacks(w, inp)]
-    ref = F.scaled_dot_product_attention(inp["q"], inp["k"], inp["v"])
+    sdpa_out = F.scaled_dot_product_attention(inp["q"], inp["k"], inp["v"])
     ro, rl = oracle.usp_forward(*[f64(t) for t in _stacks(w, inp)], w.ulysses, w.ring, w.scale)
     plain_o, plain_l = usp.attn_chunk_fwd(inp["q"].cuda(), inp["k"].cuda(), inp["v"].cuda(), w.scale)
     for mode in ("materialised", "fused"):
         o, l = _run(w, st, mode)
         check_out(o, l, ro, rl, "f32", f"demo {mode}")
         full = wl.from_token_stack(o.cpu())
-        assert torch.allclose(full, ref, atol=gd["atol"]) == gd["printed_result"]
+        assert torch.allclose(full, sdpa_out, atol=gd["atol"]) == gd["printed_result"]
         if mode == "materialised":
             assert torch.equal(full, plain_o.cpu())
             assert torch.equal(wl.from_token_stack(l.cpu()), plain_l.cpu())

@@ -117,14 +117,29 @@ def test_merge_special_cases():
 
 # ----------------------------------------------------------------- re-layout
 
-def _page_all_to_all_heads(shards, H, P):
-    """Per destination card r: head group r of every source card, concatenated
-    along tokens in source order (the handbook's all_to_all_heads, restated)."""
-    return [torch.cat([t[:, r * H // P:(r + 1) * H // P] for t in shards], dim=2) for r in range(P)]
+def _heads_exchange(shards, H, P):
+    """The handbook's head exchange, built independently of the oracle's run
+    loops from tensor views: P source cards each hold [B, H, n, D] (their
+    tokens, every head); destination card j receives head group j of every
+    source, the sources' token segments laid end to end in source order.
+    Stack the sources, split H into (P, H/P), and move the destination axis
+    to the front and the source axis next to the token axis."""
+    S = torch.stack(shards)                                   # [src, B, H, n, D]
+    src, B, _, n, D = S.shape
+    S = S.reshape(src, B, P, H // P, n, D)                    # [src, B, dst, h', n, D]
+    S = S.permute(2, 1, 3, 0, 4, 5)                           # [dst, B, h', src, n, D]
+    return list(S.reshape(P, B, H // P, src * n, D))          # per dst: [B, h', src*n, D]
 
 
-def _page_all_to_all_tokens(parts, N, P):
-    return [torch.cat([t[:, :, r * N // P:(r + 1) * N // P] for t in parts], dim=1) for r in range(P)]
+def _tokens_exchange(parts, N, P):
+    """The inverse exchange: P cards each hold [B, H/P, N, D] (all tokens of
+    their head group); source card s receives token segment s of every card's
+    heads, the head groups stacked in card order."""
+    S = torch.stack(parts)                                    # [grp, B, h', N, D]
+    grp, B, hp, _, D = S.shape
+    S = S.reshape(grp, B, hp, P, N // P, D)                   # [grp, B, h', seg, n, D]
+    S = S.permute(3, 1, 0, 2, 4, 5)                           # [seg, B, grp, h', n, D]
+    return list(S.reshape(P, B, grp * hp, N // P, D))        # per seg: [B, H, n, D]
 
 
 @pytest.mark.parametrize("u,r,B,H,N,D", [(4, 1, 1, 8, 256, 32), (2, 2, 2, 6, 24, 3), (3, 2, 1, 9, 42, 5), (1, 3, 1, 2, 9, 4), (2, 1, 1, 2, 2, 1)])
@@ -135,10 +150,10 @@ def test_relayout_matches_page_construction(u, r, B, H, N, D):
     X = uo.tok2head(T.numpy(), u, r)
     for g in range(r):
         shards = [x[:, :, (g * u + s) * Ns:(g * u + s + 1) * Ns] for s in range(u)]
-        ref = _page_all_to_all_heads(shards, H, u)
+        ref = _heads_exchange(shards, H, u)
         for j in range(u):
             assert torch.equal(torch.from_numpy(X[g, j]), ref[j])
-        back = _page_all_to_all_tokens([torch.from_numpy(X[g, j]) for j in range(u)], Nr, u)
+        back = _tokens_exchange([torch.from_numpy(X[g, j]) for j in range(u)], Nr, u)
         Tb = uo.head2tok(X, u, r)
         for s in range(u):
             assert torch.equal(torch.from_numpy(Tb[g, s]), back[s])
@@ -173,8 +188,8 @@ def test_page_demo_golden():
     Tq, Tk, Tv = (wl.to_token_stack(inp[n], w.ulysses, w.ring).numpy() for n in ("q", "k", "v"))
     O, L = uo.usp_forward(Tq, Tk, Tv, w.ulysses, w.ring, w.scale)
     full = wl.from_token_stack(torch.from_numpy(O))
-    ref = F.scaled_dot_product_attention(q0, k0, v0)
-    assert torch.allclose(full.float(), ref, atol=gd["atol"]) == gd["printed_result"]
+    sdpa_o = F.scaled_dot_product_attention(q0, k0, v0)
+    assert torch.allclose(full.float(), sdpa_o, atol=gd["atol"]) == gd["printed_result"]
     ro, rl = _sdpa(q0.double(), k0.double(), v0.double(), w.scale)
     np.testing.assert_allclose(full.numpy(), ro.numpy(), atol=1e-12)
     np.testing.assert_allclose(wl.from_token_stack(torch.from_numpy(L)).numpy(), rl.numpy(), atol=1e-12)
@@ -396,7 +411,7 @@ def _pins_pass(mod) -> bool:
             Ns = 12 // (u * r)
             for g in range(r):
                 sh = [x[:, :, (g * u + s) * Ns:(g * u + s + 1) * Ns] for s in range(u)]
-                ref = _page_all_to_all_heads(sh, 4, u)
+                ref = _heads_exchange(sh, 4, u)
                 if not all(torch.equal(torch.from_numpy(X[g, j]), ref[j]) for j in range(u)):
                     return False
             if not np.array_equal(mod.head2tok(X, u, r), T):
