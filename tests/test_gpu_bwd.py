@@ -128,26 +128,29 @@ def _small_bwd_inputs(seed=21):
     return w, st
 
 
-def test_bwd_concurrent_kernels_graph_capture():
+@pytest.mark.parametrize("mode", ["fused", "materialised"])
+def test_bwd_concurrent_kernels_graph_capture(mode):
     """The backward's dQ kernel runs on a library-owned side stream, forked and
     joined with events: captured into a CUDA graph and replayed it must give
-    the eager result bit for bit."""
+    the eager result bit for bit (the materialised call adds its re-layouts
+    to the graph)."""
     usp = _usp()
     w, st = _small_bwd_inputs()
     o, l = usp.attention_fwd(st["q"], st["k"], st["v"], 2, 2, w.scale, mode="fused")
-    ref = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+    ref = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, mode=mode)
     torch.cuda.synchronize()
-    ws = torch.empty(usp.workspace_bytes(w.B, w.H, w.N, w.D, 2, 2, torch.bfloat16, backward=True),
+    ws = torch.empty(usp.workspace_bytes(w.B, w.H, w.N, w.D, 2, 2, torch.bfloat16, mode=mode, backward=True),
                      dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):   # warm-up on the capture stream
-        usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, workspace=ws)
+        usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, workspace=ws, mode=mode)
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        got = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, workspace=ws)
+        got = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, workspace=ws,
+                                mode=mode)
     for _ in range(2):
         for t in got:
             t.zero_()
@@ -158,14 +161,15 @@ def test_bwd_concurrent_kernels_graph_capture():
     assert usp.device_status() == 0
 
 
-def test_bwd_two_host_threads():
+@pytest.mark.parametrize("mode", ["fused", "materialised"])
+def test_bwd_two_host_threads(mode):
     """Two host threads, each on its own stream, share the device's side stream
     (it is locked per call): every result equals the single-thread one."""
     import threading
     usp = _usp()
     w, st = _small_bwd_inputs(seed=22)
     o, l = usp.attention_fwd(st["q"], st["k"], st["v"], 2, 2, w.scale, mode="fused")
-    ref = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+    ref = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, mode=mode)
     torch.cuda.synchronize()
     errors = []
 
@@ -174,7 +178,7 @@ def test_bwd_two_host_threads():
             s = torch.cuda.Stream()
             with torch.cuda.stream(s):
                 for _ in range(8):
-                    got = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale)
+                    got = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], 2, 2, w.scale, mode=mode)
                     s.synchronize()
                     for a, b in zip(got, ref):
                         if not torch.equal(a.view(torch.int16), b.view(torch.int16)):
