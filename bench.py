@@ -674,7 +674,7 @@ def our_arm(args, w, ws, rank, local):
         if "GB/s" in r:
             r["frac_of_hbm"] = r["GB/s"] / peaks["hbm_gbs"]
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:   # the oracle baseline is taken on rank 0 of a 1-GPU run only
         heads = sample_heads(w)
         dt = run_oracle_sample(w, heads)
         cpu = {"value": oracle_sample_flop(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
