@@ -249,6 +249,7 @@ class Step:
         nws = usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, "materialised")
         self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
         self.backward = backward
+        self.bwd_phases = False   # record the library's phase events around the backward (timed loop only)
         if backward:
             nb = usp.workspace_bytes(w.B, w.H, w.N, w.D, w.ulysses, w.ring, w.torch_dtype, backward=True)
             self.ws_b = torch.empty(nb, dtype=torch.uint8, device="cuda")
@@ -320,7 +321,14 @@ class Step:
         if ev:
             ev[2].record()
         if self.backward and only in (None, "backward"):
+            # phase events only around the backward: events between the
+            # forward's kernels would stop each from starting under the
+            # previous one's tail (programmatic dependent launch)
+            if self.bwd_phases:
+                self.usp.lib().usp_profile_phases(1)
             self.bwd()
+            if self.bwd_phases:
+                self.usp.lib().usp_profile_phases(0)
         if ev:
             ev[3].record()
 
@@ -593,8 +601,7 @@ def our_arm(args, w, ws, rank, local):
     import ctypes
     phase_ms = (ctypes.c_float * 8)()
     bwd_phases = []                      # per step: [prep, dK/dV kernel, dQ kernel] ms
-    if step.backward:
-        _lib_check(L.usp_profile_phases(1))
+    step.bwd_phases = step.backward
     with ClockSampler(local) as clocks:
         for _ in range(args.warmup):
             step.flush()
@@ -613,8 +620,8 @@ def our_arm(args, w, ws, rank, local):
                 bwd_phases.append([phase_ms[k] * 1e-3 for k in range(n)])
         torch.cuda.synchronize()
         clocks.mark("end")
-    if step.backward:
-        _lib_check(L.usp_profile_phases(0))
+    step.bwd_phases = False
+    _lib_check(L.usp_profile_phases(0))
     barrier(ws)
     if usp.device_status() != 0:
         raise RuntimeError("device error status during the timed steps")

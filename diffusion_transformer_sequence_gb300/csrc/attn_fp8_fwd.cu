@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  ptx::griddep_wait();    // the prologue above overlapped the quantisation's tail
+  ptx::griddep_launch();
   const uint32_t tmem = *tmem_slot;
   const Guard& G = p.guard;
   if (warp < 4) {
@@ -406,8 +408,7 @@ cudaError_t launch_attn_fp8_fwd(const Fp8AttnArgs& a, const Guard& g, cudaStream
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.guard = g;
   dim3 grid((unsigned)((p.tiles + 1) / 2), (unsigned)a.BH, 1);
-  attn_fp8_fwd_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mvt, p);
-  return cudaGetLastError();
+  return launch_pdl(attn_fp8_fwd_kernel, grid, dim3(NUM_THREADS), SMEM_BYTES, stream, mq, mk, mvt, p);
 }
 
 }  // namespace usp

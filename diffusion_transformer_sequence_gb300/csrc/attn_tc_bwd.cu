@@ -219,6 +219,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const TileRef kt = tile_ref(p, blockIdx.x, jseg);
   const Guard& G = p.guard;
   const uint32_t tmem = prologue(smem, sbase, warp);
+  ptx::griddep_wait();    // the prologue above overlapped the previous kernel's tail
+  ptx::griddep_launch();
   const uint32_t tSt = tmem, tdPt = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
   const int T = p.tiles;
 
@@ -612,6 +614,8 @@ __global__ void __launch_bounds__(256) usp_bwd_prep_kernel(const __nv_bfloat16* 
                                                            const float* __restrict__ lse, float* __restrict__ delta,
                                                            float* __restrict__ l2, int64_t rows, int64_t Ns,
                                                            int64_t Ns_pad) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = gt / 16;
   const int part = (int)(gt % 16);
@@ -683,9 +687,9 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   if (ea != cudaSuccess) return ea;
   const int64_t rows = a.BH * a.sp * a.Ns;
   const int64_t Ns_pad = (a.Ns + 3) / 4 * 4;
-  usp_bwd_prep_kernel<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, stream>>>(
-      (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, a.delta, a.l2, rows, a.Ns, Ns_pad);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(usp_bwd_prep_kernel, dim3((unsigned)((rows * 16 + 255) / 256)), dim3(256), 0, stream,
+                             (const __nv_bfloat16*)a.out, (const __nv_bfloat16*)a.dout, a.lse, a.delta, a.l2, rows,
+                             a.Ns, Ns_pad);
   if (e != cudaSuccess) return e;
   const int prep_mark = phase_mark(stream);
   CUtensorMap mq, mk, mv, mdo, ml2, mdl;
@@ -715,8 +719,7 @@ cudaError_t launch_attn_tc_bwd(const TcBwdArgs& a, const Guard& g, cudaStream_t 
   BwdParams pq = p;
   p.dst0 = a.dk;
   p.dst1 = a.dv;
-  usp_bwd_dkdv_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, mdo, ml2, mdl, p);
-  e = cudaGetLastError();
+  e = launch_pdl(usp_bwd_dkdv_kernel, grid, dim3(NUM_THREADS), SMEM_BYTES, stream, mq, mk, mv, mdo, ml2, mdl, p);
   phase_mark(stream, prep_mark);
   pq.dst0 = a.dq;
   pq.dst1 = nullptr;

@@ -228,6 +228,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  ptx::griddep_wait();    // the prologue above overlapped the previous kernel's tail
+  ptx::griddep_launch();
   const uint32_t tmem = *tmem_slot;
   const Guard& G = p.guard;
   // Register split: the producer/MMA warpgroup hands registers to the two
@@ -595,11 +597,10 @@ cudaError_t launch_attn_tc_fwd(const AttnArgs* sides, int nsides, const Guard& g
   if (ctas < 1 || ctas > 2147483647LL) return cudaErrorInvalidValue;
   dim3 grid((unsigned)ctas, 1, 1);
   if (p.kv2.tiles > 0)
-    attn_tc_fwd_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq[0], mq[1], mkv.k, mkv.v, mkv.k2, mkv.v2, p);
-  else
-    attn_tc_fwd_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(mq[0], mq[1], mkv.k, mkv.v, mkv.k2, mkv.v2,
-                                                                          p);
-  return cudaGetLastError();
+    return launch_pdl(attn_tc_fwd_kernel<true>, grid, dim3(NUM_THREADS), SMEM_BYTES, stream, mq[0], mq[1], mkv.k,
+                      mkv.v, mkv.k2, mkv.v2, p);
+  return launch_pdl(attn_tc_fwd_kernel<false>, grid, dim3(NUM_THREADS), SMEM_BYTES, stream, mq[0], mq[1], mkv.k,
+                    mkv.v, mkv.k2, mkv.v2, p);
 }
 
 }  // namespace usp

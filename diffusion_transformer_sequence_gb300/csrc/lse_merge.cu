@@ -11,6 +11,7 @@
 // one row + one LSE.
 #include <cuda_bf16.h>
 
+#include "ptx.cuh"
 #include "usp_internal.cuh"
 
 namespace usp {
@@ -67,6 +68,8 @@ __global__ void __launch_bounds__(256) merge_vec_kernel(const T* __restrict__ ou
                                                         const float* __restrict__ lses, int R,
                                                         T* __restrict__ out, float* __restrict__ lse,
                                                         int64_t rows, int64_t D) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int64_t tpr = D / 8;
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t row = gt / tpr;
@@ -118,6 +121,8 @@ __global__ void __launch_bounds__(256) merge_scalar_kernel(const T* __restrict__
                                                            const float* __restrict__ lses, int R,
                                                            T* __restrict__ out, float* __restrict__ lse,
                                                            int64_t rows, int64_t D) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (gt >= rows * D) return;
   const int64_t row = gt / D;
@@ -140,17 +145,14 @@ cudaError_t launch_typed(const void* outs, const float* lses, int R, void* out, 
   if (vec) {
     const int64_t threads = rows * (D / 8);
     const int64_t blocks = (threads + 255) / 256;
-    if (R <= 2)
-      merge_vec_kernel<T, 2><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
-    else if (R <= 4)
-      merge_vec_kernel<T, 4><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
-    else
-      merge_vec_kernel<T, 8><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
-  } else {
-    const int64_t blocks = (rows * D + 255) / 256;
-    merge_scalar_kernel<T><<<(unsigned)blocks, 256, 0, stream>>>((const T*)outs, lses, R, (T*)out, lse, rows, D);
+    const dim3 g((unsigned)blocks), b(256);
+    if (R <= 2) return launch_pdl(merge_vec_kernel<T, 2>, g, b, 0, stream, (const T*)outs, lses, R, (T*)out, lse, rows, D);
+    if (R <= 4) return launch_pdl(merge_vec_kernel<T, 4>, g, b, 0, stream, (const T*)outs, lses, R, (T*)out, lse, rows, D);
+    return launch_pdl(merge_vec_kernel<T, 8>, g, b, 0, stream, (const T*)outs, lses, R, (T*)out, lse, rows, D);
   }
-  return cudaGetLastError();
+  const int64_t blocks = (rows * D + 255) / 256;
+  return launch_pdl(merge_scalar_kernel<T>, dim3((unsigned)blocks), dim3(256), 0, stream, (const T*)outs, lses, R,
+                    (T*)out, lse, rows, D);
 }
 
 }  // namespace

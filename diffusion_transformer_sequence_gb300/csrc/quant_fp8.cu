@@ -81,6 +81,8 @@ struct Dsts3 {
 // Codes in the input layout, 16 elements per thread.
 __global__ void __launch_bounds__(kThreads) quant_kernel(Srcs3 srcs, Dsts3 dsts, const unsigned* __restrict__ amax,
                                                          int64_t BH, int64_t block_elems, int64_t total) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int z = blockIdx.y;
   const int64_t e = ((int64_t)blockIdx.x * kThreads + threadIdx.x) * 16;
   if (e >= total) return;
@@ -112,6 +114,8 @@ __global__ void __launch_bounds__(kThreads) quant_vt_kernel(const __nv_bfloat16*
                                                             const unsigned* __restrict__ amax_v, int64_t BH,
                                                             int64_t Ns, int64_t Ns_pad) {
   __shared__ __align__(16) uint32_t tile[128 * 32];
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int64_t key0 = (int64_t)blockIdx.x * 128;
   const int64_t bh = blockIdx.y, s = blockIdx.z;
   const float inv = inv_scale(__ldg(amax_v + bh));
@@ -188,8 +192,7 @@ cudaError_t launch_quant(const void* const* srcs, uint8_t* const* dsts, const in
   }
   const int64_t total = sp * BH * Ns * D;
   dim3 grid((unsigned)((total / 16 + kThreads - 1) / kThreads), (unsigned)count, 1);
-  quant_kernel<<<grid, kThreads, 0, stream>>>(s, d, amax, BH, Ns * D, total);
-  return cudaGetLastError();
+  return launch_pdl(quant_kernel, grid, dim3(kThreads), 0, stream, s, d, amax, BH, Ns * D, total);
 }
 
 }  // namespace
@@ -218,9 +221,8 @@ cudaError_t launch_quantize_qkv_fp8(const void* q, const void* k, const void* v,
   e = launch_quant(srcs, dsts, tensor, 2, amax, BH, sp, Ns, 128, stream);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((Ns + 127) / 128), (unsigned)BH, (unsigned)sp);
-  quant_vt_kernel<<<grid, kThreads, 0, stream>>>(static_cast<const __nv_bfloat16*>(v), vt8, amax + 2 * BH, BH, Ns,
-                                                  fp8_vt_pitch(Ns));
-  return cudaGetLastError();
+  return launch_pdl(quant_vt_kernel, grid, dim3(kThreads), 0, stream, static_cast<const __nv_bfloat16*>(v), vt8,
+                    (const unsigned*)(amax + 2 * BH), BH, Ns, fp8_vt_pitch(Ns));
 }
 
 }  // namespace usp

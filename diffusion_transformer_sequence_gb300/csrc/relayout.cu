@@ -11,6 +11,7 @@
 // the widest aligned vector (16 bytes on every workload) and several loads in
 // flight per thread; staging through shared memory would add a copy without
 // improving coalescing.  Run-level index arithmetic happens once per CTA.
+#include "ptx.cuh"
 #include "usp_internal.cuh"
 
 namespace usp {
@@ -36,6 +37,8 @@ struct Tensors {
 template <typename Vec, bool kTok2Head>
 __global__ void __launch_bounds__(kThreads) relayout_kernel(const __grid_constant__ Tensors ts, int64_t nruns,
                                                             int64_t B, int64_t H, int64_t Hu, int64_t u) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
   const int64_t run_vecs = ts.run_vecs[blockIdx.z];
   if ((int64_t)blockIdx.x * kThreads * kUnroll >= run_vecs) return;  // a shorter tensor of the launch
   const Vec* __restrict__ src = static_cast<const Vec*>(ts.src[blockIdx.z]);
@@ -93,11 +96,8 @@ cudaError_t launch_vec(Tensors ts, int count, int64_t nruns, const int64_t* run_
   if (gx > 1024) gx = 1024;
   int64_t gy = nruns < 65535 ? nruns : 65535;
   dim3 grid((unsigned)gx, (unsigned)gy, (unsigned)count);
-  if (tok2head)
-    relayout_kernel<Vec, true><<<grid, kThreads, 0, stream>>>(ts, nruns, B, H, Hu, u);
-  else
-    relayout_kernel<Vec, false><<<grid, kThreads, 0, stream>>>(ts, nruns, B, H, Hu, u);
-  return cudaGetLastError();
+  if (tok2head) return launch_pdl(relayout_kernel<Vec, true>, grid, dim3(kThreads), 0, stream, ts, nruns, B, H, Hu, u);
+  return launch_pdl(relayout_kernel<Vec, false>, grid, dim3(kThreads), 0, stream, ts, nruns, B, H, Hu, u);
 }
 
 }  // namespace

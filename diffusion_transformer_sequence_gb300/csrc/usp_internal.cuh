@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 namespace usp {
 
@@ -30,6 +31,28 @@ inline cudaError_t smem_limit_once(std::atomic<unsigned long long>& done, const 
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
   return e;
+}
+
+// Launches `kernel` on `stream` with programmatic stream serialisation: its
+// CTAs may start (prologue: barriers, TMEM, tensor-map prefetch) while the
+// previous kernel of the stream drains its last wave.  Every kernel launched
+// this way calls ptx::griddep_wait() before its first access to global
+// memory, so it neither reads what that kernel writes nor overwrites what it
+// reads before that kernel has completed.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Per-launch guard: where to record an expired wait, and the wait limits.
