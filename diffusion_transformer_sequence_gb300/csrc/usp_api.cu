@@ -838,7 +838,7 @@ int usp_profile_phases(int enable) {
     t_phase.created = true;
   }
   t_phase.enabled = enable != 0;
-  t_phase.marks = 0;
+  if (enable) t_phase.marks = 0;  // disabling keeps the last recorded call readable
   return USP_OK;
 }
 

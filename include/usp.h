@@ -300,7 +300,10 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *                         [text-query merge]
  * (the fp32 fused forward and usp_attention_bwd record nothing; the fp32
  * materialised backward records [tok2head] [backward] [head2tok]).  The events
- * are created by the library on first enable.  Returns USP_OK or USP_ERR_CUDA. */
+ * are created by the library on first enable; enabling starts a fresh
+ * record, disabling keeps the most recent call's record readable.  While
+ * enabled, the events between a call's kernels also stop each kernel from
+ * starting under the previous one's tail.  Returns USP_OK or USP_ERR_CUDA. */
 int usp_profile_phases(int enable);
 
 /* Waits for the last event of the most recent recorded call on this thread
