@@ -258,9 +258,12 @@ class Step:
             usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
                               mode="fused", out=self.out_f, lse=self.lse_f)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-        # materialised: tok2head (q, k, v in one launch), chunk attention, merge (ring > 1), head2tok x2;
-        # fused: one; backward: prep + dK/dV + dQ
-        self.launches_per_step = (5 if w.ring > 1 else 4) + 1 + (3 if backward else 0)
+        # materialised: tok2head (q, k, v in one launch), chunk attention, merge (ring > 1), head2tok of out
+        # and lse (one launch when both move in 16-byte vectors, else two); fused: one; backward: prep +
+        # dK/dV + dQ
+        elt = 2 if w.dtype == "bf16" else 4
+        h2t = 1 if (w.Ns * 4) % 16 == 0 and (w.Ns * w.D * elt) % 16 == 0 else 2
+        self.launches_per_step = 2 + (1 if w.ring > 1 else 0) + h2t + 1 + (3 if backward else 0)
         self.joint = w.Nt > 0
         if self.joint:
             # text tokens replicated on every virtual rank: q_txt, k_txt, v_txt [B, H, Nt, D]
@@ -274,8 +277,8 @@ class Step:
                                             "materialised", True)
             self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
             # materialised: tok2head, partials against the image chunks, partials against the text,
-            # merge, head2tok x2, text merge; fused: one launch (image and text queries)
-            self.launches_per_step = 7 + 1
+            # merge, head2tok of out and lse, text merge; fused: one launch (image and text queries)
+            self.launches_per_step = 5 + h2t + 1
 
     def flop(self):
         if self.joint:
