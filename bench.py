@@ -377,10 +377,11 @@ class Step:
 
     def run_e2e_pipelined(self, steps):
         """End to end with host buffers, software-pipelined over three streams:
-        step i's host->device copy of its inputs (pinned), its compute (L2
-        flushed first, as in the device-timed loop) and the device->host copy
-        of its results run on separate streams with two device buffer sets,
-        so step i+1's inputs arrive and step i-1's results leave while step i
+        step i's host->device copy of its inputs (pinned) followed by the L2
+        flush (so the inputs are evicted before step i starts, as in the
+        device-timed loop), its compute, and the device->host copy of its
+        results run on separate streams with two device buffer sets, so step
+        i+1's inputs arrive and step i-1's results leave while step i
         computes.  Every step still moves its own inputs in and results out.
         Returns the elapsed seconds from before the first copy to after the
         last result has landed in host memory."""
@@ -402,11 +403,11 @@ class Step:
             with torch.cuda.stream(s_in):
                 for n in self.inputs():
                     self.dev[n].copy_(self.host[n], non_blocking=True)
+                self.flush(hold=False)                # evicts the inputs just copied
                 in_ready[k].record(s_in)
             s_cmp.wait_event(in_ready[k])
             if i >= 2:
                 s_cmp.wait_event(out_free[k])         # step i-2's results have left set k
-            self.flush(hold=False)
             self.fwd("materialised")
             self.fwd("fused")
             if self.backward:
@@ -656,8 +657,9 @@ def our_arm(args, w, ws, rank, local):
         h2d, d2h = step.io_bytes()
         e2e = {"value": ws * step.flop() / e2e_s / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-               "how": "pinned host buffers; per step H2D of the inputs, the step (L2 flushed first) and D2H of "
-                      "every result on three streams, two device buffer sets (steps overlap)"}
+               "how": "pinned host buffers; per step H2D of the inputs then the L2 flush (on the copy stream, "
+                      "before the step starts), the step, and D2H of every result, on three streams with two "
+                      "device buffer sets (steps overlap)"}
 
     rows = time_rows(w) if (rank == 0 and not args.no_rows) else {}
     if rank != 0:
