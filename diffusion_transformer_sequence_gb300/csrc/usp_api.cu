@@ -565,15 +565,30 @@ int usp_attention_fwd_joint(const void* q, const void* k, const void* v, const v
     cudaError_t e = launch_relayout_n(srcs, dsts, 3, B, H, Ns, D, u, r, elt, true, s);
     if (e != cudaSuccess) return cuda_fail(e);
     if (prof) phase_mark(s);
-    AttnArgs A[2] = {img_img, txt_img};
-    if ((st = run_attention(A, tq ? 2 : 1, dtype, D, s)) != USP_OK) return st;
   }
   {
+    // The two attention launches read the re-laid inputs and write disjoint
+    // partial planes: the short second one (every query set against the
+    // text) runs on the device's side stream, so its CTAs fill the first
+    // one's last wave instead of waiting behind it.
+    AttnArgs A[2] = {img_img, txt_img};
     AttnArgs Bt[2];
     int n = 0;
     if (N > 0) Bt[n++] = img_txt;
     if (tq) Bt[n++] = txt_txt;
-    if (n > 0 && (st = run_attention(Bt, n, dtype, D, s)) != USP_OK) return st;
+    cudaStream_t side = s;
+    const bool fork = N > 0 && n > 0;
+    if (fork) {
+      cudaError_t e = side_begin(s, &side);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if (N > 0) st = run_attention(A, tq ? 2 : 1, dtype, D, s);
+    if (st == USP_OK && n > 0) st = run_attention(Bt, n, dtype, D, side);
+    if (fork) {
+      const cudaError_t j = side_end(s);  // always join, also after a failed launch
+      if (st == USP_OK && j != cudaSuccess) st = cuda_fail(j);
+    }
+    if (st != USP_OK) return st;
   }
   if (prof) phase_mark(s);
   if (N > 0) {

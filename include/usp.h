@@ -203,7 +203,10 @@ size_t usp_attention_joint_workspace_bytes(int64_t B, int64_t H, int64_t N, int6
  *     of head group j -> merge of ring + 1 partials -> head2tok.  Text
  *     queries of head group j: one partial per ring chunk c of that group
  *     (the same on every ring rank, computed once) plus one against the
- *     text K/V -> merge into out_txt, lse_txt.
+ *     text K/V -> merge into out_txt, lse_txt.  The launch of the partials
+ *     against the text runs on the library-owned stream of the current
+ *     device that usp_attention_bwd uses, forked from and joined back to
+ *     `stream` with events (the call stays ordered on `stream`).
  *   USP_FUSED: one kernel launch reads the stacks and the text in place
  *     (image and text queries share it); the text K/V are the last KV tiles
  *     of the online softmax.
