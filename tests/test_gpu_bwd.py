@@ -121,6 +121,36 @@ def test_bwd_wan_shapes_sampled():
     _check_grad(g_dv, r_dv, "bf16", "wan dv")
 
 
+def test_bwd_wan720p_sampled():
+    """Wan 720p (B1 H40 N75600 D128, u8 x r2; Ns = 4725, so every shard ends in
+    a ragged tile), forward + both backward calls on the GPU against the
+    oracle at 2048 sampled query rows (dq) and 2048 sampled key rows (dk, dv)
+    of two heads on either side of a Ulysses head-group boundary."""
+    usp = _usp()
+    w = wl.WORKLOADS["wan720p"]
+    inp = wl.make_inputs(w, with_dout=True)
+    st = {n: wl.to_token_stack(t, w.ulysses, w.ring).cuda() for n, t in inp.items()}
+    o, l = usp.attention_fwd(st["q"], st["k"], st["v"], w.ulysses, w.ring, w.scale, mode="fused")
+    heads = [4, 5]   # Hu = 5
+    qrows = wl.sample_rows(w, 2048)
+    g = torch.Generator().manual_seed(w.row_seed + 2)
+    krows = torch.unique(torch.cat([qrows[::2], torch.randperm(w.N, generator=g)[:1024]]))
+    flat = {n: inp[n].reshape(w.B * w.H, w.N, w.D) for n in inp}
+    f = lambda n: flat[n][heads].float().numpy()
+    r_dq, r_dk, r_dv = pool.sampled_backward(f("q"), f("k"), f("v"), f("dout"), w.scale, list(range(len(heads))),
+                                             qrows.numpy(), krows.numpy())
+    for mode in ("fused", "materialised"):
+        dq, dk, dv = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], w.ulysses, w.ring, w.scale,
+                                       mode=mode)
+        assert usp.device_status() == 0
+        sel = lambda t, rows: wl.from_token_stack(t).reshape(w.B * w.H, w.N, w.D)[heads][:, rows.cuda()]
+        _check_grad(sel(dq, qrows), r_dq, "bf16", f"wan720p {mode} dq")
+        _check_grad(sel(dk, krows), r_dk, "bf16", f"wan720p {mode} dk")
+        _check_grad(sel(dv, krows), r_dv, "bf16", f"wan720p {mode} dv")
+        del dq, dk, dv
+        torch.cuda.empty_cache()
+
+
 def _small_bwd_inputs(seed=21):
     w = wl.custom("bwdc", "bf16", 1, 4, 1024, 128, 2, 2, seed=seed, backward=True)
     inp = wl.make_inputs(w)

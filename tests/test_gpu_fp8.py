@@ -94,7 +94,7 @@ def test_fp8_attention_small_full_rows(B, H, N, u, r):
     check_fp8(f64(go), f64(gl), ro, rl, sig, f"fp8 B{B} H{H} N{N} u{u} r{r}")
 
 
-@pytest.mark.parametrize("name,heads", [("qwen1024", None), ("wan_s32k", [0, 4, 5, 39])])
+@pytest.mark.parametrize("name,heads", [("qwen1024", None), ("wan_s32k", [0, 4, 5, 39]), ("wan720p", [4, 5])])
 def test_fp8_attention_workloads_sampled(name, heads):
     usp = _usp()
     w = wl.WORKLOADS[name]
