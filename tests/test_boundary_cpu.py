@@ -26,6 +26,46 @@ def test_exports_every_declared_symbol(L):
     assert set(declared) == set(_lib.SIGNATURES), "binding signatures out of sync with usp.h"
 
 
+def _header_prototypes():
+    """name -> list of (C type of each parameter) parsed from include/usp.h."""
+    import re
+    from diffusion_transformer_sequence_gb300 import _lib
+    txt = open(_lib.HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", " ", txt, flags=re.S)          # drop comments
+    protos = {}
+    for m in re.finditer(r"([A-Za-z_][A-Za-z0-9_ \*]*?)\b(usp_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", txt):
+        args = [a.strip() for a in re.sub(r"\s+", " ", m.group(3)).split(",")]
+        protos[m.group(2)] = [] if args == ["void"] or args == [""] else args
+    return protos
+
+
+def test_binding_signatures_match_header():
+    """Every ctypes signature has the header's parameter count, and each
+    parameter's ctypes type has the width and kind of its C type."""
+    import ctypes
+    from diffusion_transformer_sequence_gb300 import _lib
+    protos = _header_prototypes()
+    assert set(protos) == set(_lib.SIGNATURES)
+    for name, (res, args) in _lib.SIGNATURES.items():
+        cargs = protos[name]
+        assert len(cargs) == len(args), f"{name}: header has {len(cargs)} parameters, binding {len(args)}"
+        for c, t in zip(cargs, args):
+            ctype = c.rsplit(" ", 1)[0]
+            if "*" in c or "usp_stream_t" in c:   # every pointer (and the stream handle) passes as an address
+                assert t is ctypes.c_void_p or issubclass(t, ctypes._Pointer), \
+                    f"{name}: pointer parameter {c!r} bound as {t}"
+            elif "int64_t" in ctype:
+                assert t is ctypes.c_int64, f"{name}: {c!r} bound as {t}"
+            elif "size_t" in ctype:
+                assert t is ctypes.c_size_t, f"{name}: {c!r} bound as {t}"
+            elif "float" in ctype:
+                assert t is ctypes.c_float, f"{name}: {c!r} bound as {t}"
+            elif "long long" in ctype:
+                assert t is ctypes.c_longlong, f"{name}: {c!r} bound as {t}"
+            else:   # int and the enums (usp_dtype, usp_mode)
+                assert t is ctypes.c_int, f"{name}: {c!r} bound as {t}"
+
+
 def test_status_strings(L):
     from diffusion_transformer_sequence_gb300 import _lib
     for code, name in [(0, "USP_OK"), (1, "USP_ERR_INVALID_ARG"), (2, "USP_ERR_DIVISIBILITY"),
