@@ -150,19 +150,38 @@ def oracle_sample_flop(w, heads):
 
 def run_oracle_sample(w, heads: int):
     """Time the CPU oracle's USP forward (joint when the workload has text
-    tokens) on `heads` heads of the workload."""
+    tokens) on `heads` heads of the workload.  Returns (seconds, parity):
+    the same sub-problem also runs through the fused call on the GPU, and
+    parity holds the largest |out| and relative lse differences between
+    the two (image queries)."""
     import oracle
+    import diffusion_transformer_sequence_gb300 as usp
     sub = wl.custom(w.name, w.dtype, w.B, heads, w.N, w.D, w.ulysses, w.ring, seed=w.seed, Nt=w.Nt)
     inp = wl.make_inputs(sub, with_dout=False)
-    stacks = [wl.to_token_stack(inp[n], w.ulysses, w.ring).double().numpy() for n in ("q", "k", "v")]
+    st = [wl.to_token_stack(inp[n], w.ulysses, w.ring) for n in ("q", "k", "v")]
+    stacks = [t.double().numpy() for t in st]
     t0 = time.perf_counter()
     if w.Nt:
-        txt = {n: t.double().numpy() for n, t in wl.make_text_inputs(sub).items()}
-        oracle.usp_forward_joint(*stacks, txt["k_txt"], txt["v_txt"], w.ulysses, w.ring, w.scale,
-                                 q_txt=txt["q_txt"])
+        txt_t = wl.make_text_inputs(sub)
+        txt = {n: t.double().numpy() for n, t in txt_t.items()}
+        ro, rl = oracle.usp_forward_joint(*stacks, txt["k_txt"], txt["v_txt"], w.ulysses, w.ring, w.scale,
+                                          q_txt=txt["q_txt"])[:2]
     else:
-        oracle.usp_forward(*stacks, w.ulysses, w.ring, w.scale)
-    return time.perf_counter() - t0
+        ro, rl = oracle.usp_forward(*stacks, w.ulysses, w.ring, w.scale)
+    dt = time.perf_counter() - t0
+    dev = [t.cuda() for t in st]
+    if w.Nt:
+        go, gl = usp.attention_fwd_joint(*dev, txt_t["k_txt"].cuda(), txt_t["v_txt"].cuda(), w.ulysses, w.ring,
+                                         w.scale, mode="fused")
+    else:
+        go, gl = usp.attention_fwd(*dev, w.ulysses, w.ring, w.scale, mode="fused")
+    import numpy as np
+    go, gl = go.double().cpu().numpy(), gl.double().cpu().numpy()
+    parity = {"max_abs_out": float(np.abs(go - ro).max()),
+              "max_rel_lse": float((np.abs(gl - rl) / np.maximum(np.abs(rl), 1e-30)).max()),
+              "vs": "oracle (numpy fp64) on the same sub-problem, fused call",
+              "bound": {"out_abs": 2e-2 if w.dtype == "bf16" else 1e-5, "lse_rel": 1e-3 if w.dtype == "bf16" else None}}
+    return dt, parity
 
 
 def cpu_cores():
@@ -700,10 +719,10 @@ def our_arm(args, w, ws, rank, local):
     cpu = None
     if not args.no_cpu_baseline and ws == 1:   # the oracle baseline is taken on rank 0 of a 1-GPU run only
         heads = sample_heads(w)
-        dt = run_oracle_sample(w, heads)
+        dt, parity = run_oracle_sample(w, heads)
         cpu = {"value": oracle_sample_flop(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
                "kind": "oracle", "sample": f"oracle USP forward (numpy fp64) on {heads} of {w.H} heads, full N, "
-                                           f"{dt:.1f} s"}
+                                           f"{dt:.1f} s", "parity": parity}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
