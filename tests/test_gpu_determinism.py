@@ -76,3 +76,52 @@ def test_double_run_bitwise(inputs, call):
     assert len(first) == len(second) and len(first) >= 2
     for i, (a, b) in enumerate(zip(first, second)):
         assert _same(a, b), f"{call}: output {i} differs between two runs"
+
+
+CAPTURED = ["fwd_materialised", "fwd_fused", "joint_materialised", "fp8"]
+
+
+@pytest.mark.parametrize("call", CAPTURED)
+def test_graph_capture_replays_bitwise(inputs, call):
+    """Each call captured into a CUDA graph (its launches chained by
+    programmatic dependent launch; the joint call forks its text launch onto
+    the side stream) and replayed gives the eager result bit for bit."""
+    usp = _usp()
+    w, st, tx = inputs
+    q, k, v = st["q"], st["k"], st["v"]
+    B, H, N, D = w.B, w.H, w.N, w.D
+    if call.startswith("fwd_"):
+        mode = call[4:]
+        ws = torch.empty(max(1, usp.workspace_bytes(B, H, N, D, 2, 2, torch.bfloat16, mode)), dtype=torch.uint8,
+                         device="cuda")
+        outs = (torch.empty_like(q), torch.empty(w.lse_stack_shape, device="cuda"))
+        fn = lambda: usp.attention_fwd(q, k, v, 2, 2, w.scale, mode=mode, out=outs[0], lse=outs[1], workspace=ws)
+    elif call == "joint_materialised":
+        ws = torch.empty(usp.joint_workspace_bytes(B, H, N, w.Nt, D, 2, 2, torch.bfloat16, "materialised", False),
+                         dtype=torch.uint8, device="cuda")
+        fn = lambda: usp.attention_fwd_joint(q, k, v, tx["k_txt"], tx["v_txt"], 2, 2, w.scale, mode="materialised",
+                                             workspace=ws)
+    else:
+        L = usp.lib()
+        ws = torch.empty(int(L.usp_attention_fp8_workspace_bytes(B, H, N, D, 2, 2)), dtype=torch.uint8, device="cuda")
+        outs = (torch.empty_like(q), torch.empty(w.lse_stack_shape, device="cuda"))
+        fn = lambda: usp.attention_fwd_fp8(q, k, v, 2, 2, w.scale, out=outs[0], lse=outs[1], workspace=ws)
+    ref = [t.clone() for t in fn()]
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):    # warm-up on the capture stream
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        got = fn()
+    for _ in range(2):
+        for t in got:
+            t.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(got, ref)):
+            assert _same(a, b), f"{call}: output {i} differs after graph replay"
+    assert usp.device_status() == 0
