@@ -151,6 +151,34 @@ def test_bwd_wan720p_sampled():
         torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name,heads", [("qwen1024", [0, 11, 12, 23]), ("qwen2048", [0, 5, 6, 23])])
+def test_bwd_qwen_workloads_sampled(name, heads):
+    """Qwen-Image 1024² (u2 x r2, the benchmark's step) and 2048² (u4 x r1):
+    the GPU forward feeds both backward calls at full size; 2048 sampled query
+    rows (dq) and 2048 sampled key rows (dk, dv) of four heads, two of them on
+    either side of a Ulysses head-group boundary, against the oracle."""
+    usp = _usp()
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, with_dout=True)
+    st = {n: wl.to_token_stack(t, w.ulysses, w.ring).cuda() for n, t in inp.items()}
+    o, l = usp.attention_fwd(st["q"], st["k"], st["v"], w.ulysses, w.ring, w.scale, mode="fused")
+    qrows = wl.sample_rows(w, 2048)
+    g = torch.Generator().manual_seed(w.row_seed + 3)
+    krows = torch.unique(torch.cat([qrows[::2], torch.randperm(w.N, generator=g)[:1024]]))
+    flat = {n: inp[n].reshape(w.B * w.H, w.N, w.D) for n in inp}
+    f = lambda n: flat[n][heads].float().numpy()
+    r_dq, r_dk, r_dv = pool.sampled_backward(f("q"), f("k"), f("v"), f("dout"), w.scale, list(range(len(heads))),
+                                             qrows.numpy(), krows.numpy())
+    sel = lambda t, rows: wl.from_token_stack(t).reshape(w.B * w.H, w.N, w.D)[heads][:, rows.cuda()]
+    for mode in ("fused", "materialised"):
+        dq, dk, dv = usp.attention_bwd(st["q"], st["k"], st["v"], o, l, st["dout"], w.ulysses, w.ring, w.scale,
+                                       mode=mode)
+        assert usp.device_status() == 0
+        _check_grad(sel(dq, qrows), r_dq, "bf16", f"{name} {mode} dq")
+        _check_grad(sel(dk, krows), r_dk, "bf16", f"{name} {mode} dk")
+        _check_grad(sel(dv, krows), r_dv, "bf16", f"{name} {mode} dv")
+
+
 def _small_bwd_inputs(seed=21):
     w = wl.custom("bwdc", "bf16", 1, 4, 1024, 128, 2, 2, seed=seed, backward=True)
     inp = wl.make_inputs(w)

@@ -46,9 +46,9 @@ RELAYOUT_CASES = [
     ("bf16", 2, 1, 1, 2, 6, 3),          # 2-byte path
     ("bf16", 1, 1, 1, 1, 1, 1),          # single element
     ("f32", 2, 3, 3, 4, 6, 1),           # LSE-like layout (D = 1)
-    ("bf16", 2, 2, 2, 4, 800, 128),      # bulk path: 51200-byte runs = one full + one partial 32 KB piece
-    ("f32", 2, 2, 1, 4, 64, 4),          # bulk path with 256-byte runs
-    ("f32", 2, 2, 1, 4, 64, 1),          # LSE with Ns = 16: 64-byte runs, bulk path
+    ("bf16", 2, 2, 2, 4, 800, 128),      # 51200-byte runs: several CTAs per run, partial last chunk
+    ("f32", 2, 2, 1, 4, 64, 4),          # 256-byte runs: one partly used CTA per run
+    ("f32", 2, 2, 1, 4, 64, 1),          # LSE with Ns = 16: 64-byte runs
 ]
 
 
