@@ -110,7 +110,14 @@ def test_lse_merge(dtype, R, B, H, Nq, D):
 
 F32_CHUNK = [(1, 8, 256, 256, 32), (2, 3, 37, 53, 16), (1, 2, 1, 129, 8), (1, 1, 130, 1, 4), (1, 2, 70, 300, 128)]
 BF16_CHUNK = [(1, 2, 128, 128), (1, 3, 300, 200), (2, 2, 1, 1), (1, 1, 129, 4097), (1, 4, 1000, 257),
-              (1, 1, 384, 384), (1, 2, 256, 1), (3, 1, 17, 2000)]
+              (1, 1, 384, 384), (1, 2, 256, 1), (3, 1, 17, 2000),
+              # more items (head x query-tile pair) than SMs: each CTA of the persistent
+              # grid walks several, with odd query-tile counts (a lone last tile) and
+              # 1, 2 or 3 KV tiles per item (the last one ragged), so the barrier
+              # phases wrap across items in every parity pattern
+              (2, 160, 300, 100), (2, 160, 300, 200), (1, 200, 300, 300),
+              # 32 KV tiles per item (the longest run persistent) and 33 (one CTA per item)
+              (1, 8, 1000, 4064), (1, 8, 1000, 4097)]
 
 
 @pytest.mark.parametrize("B,H,Nq,Nk,D", F32_CHUNK)
