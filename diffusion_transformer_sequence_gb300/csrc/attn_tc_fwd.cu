@@ -67,7 +67,7 @@ constexpr int B_QEMPTY = B_MMADONE + 1;
 constexpr int NUM_BARS = B_QEMPTY + 1;
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
 constexpr int OFF_ABORT = OFF_SLOT + 8;
-constexpr int OFF_EPI = OFF_ABORT + 8;        // EpiInfo (written once by thread 0)
+constexpr int OFF_EPI = OFF_ABORT + 8;        // EpiInfo (one-CTA-per-item launches)
 constexpr int SMEM_USED = OFF_EPI + 48;
 constexpr int SMEM_BYTES = SMEM_USED + 1024;  // slack for 1024-byte alignment of the base
 
@@ -107,9 +107,12 @@ struct TcParams {
 };
 
 // Where the epilogue of each query tile of the CTA writes: its first output
-// row, how many rows exist, and the out / lse base pointers.  Warp 2 (idle
-// otherwise) fills it before the CTA's first barrier, so the softmax warps
-// carry none of the query set's parameters through the KV loop.
+// row, how many rows exist, and the out / lse base pointers.  In a launch
+// with one CTA per item (possibly two query sets) warp 2, idle otherwise,
+// fills it before the CTA's first barrier, so the softmax warps carry none of
+// the query set's parameters through the KV loop; a persistent launch has one
+// query set, whose parameters sit at fixed offsets, and its softmax warps
+// compute each item's addressing after the item's KV loop.
 struct EpiInfo {
   int64_t orow0[2];
   void* out;
