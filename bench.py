@@ -1,16 +1,17 @@
 """Benchmark of the USP attention hot path on GB300.
 
 One step = one pass of every built row of the hot path over one batch of
-synthetic input of the named workload (default: Qwen-Image 1024^2, bf16,
-B1 H24 N4096 D128, ulysses 2 x ring 2):
+synthetic input of the named workload (default: the largest one, Wan 720p
+81 frames, bf16, B1 H40 N75600 D128, ulysses 8 x ring 2, with the backward):
   * usp_attention_fwd, materialised: tok2head(q,k,v) -> per-(rank, ring step)
     chunk attention -> LSE merge -> head2tok(out, lse)
   * usp_attention_fwd, fused: one kernel over the token-sharded stacks
   * usp_attention_bwd (when the workload has a backward)
 ``value`` is algorithmic attention FLOP of the step (4*B*H*N^2*D per forward,
 10*B*H*N^2*D per backward) / device time, in TFLOP/s, summed over ranks.
-Inputs (q, k, v: ~25 MB each) are smaller than L2, so L2 is flushed (a
-256 MB buffer is written) before every timed step, outside the timed events.
+L2 is flushed (a 256 MB buffer is written) before every timed step, outside
+the timed events (the Wan inputs, 774 MB each, are larger than L2 anyway;
+the Qwen-Image 1024^2 ones, 25 MB, are not).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 Under torchrun every rank runs its own replica (weak scaling, no data-path
@@ -182,6 +183,68 @@ def run_oracle_sample(w, heads: int):
               "vs": "oracle (numpy fp64) on the same sub-problem, fused call",
               "bound": {"out_abs": 2e-2 if w.dtype == "bf16" else 1e-5, "lse_rel": 1e-3 if w.dtype == "bf16" else None}}
     return dt, parity
+
+
+def oracle_rows_baseline(w, step, heads, nrows, cores):
+    """CPU-baseline leg for workloads too large for a full-head oracle run.
+
+    The oracle's attention of ``nrows`` seeded query rows (always including
+    shard and tile boundaries) of each listed head against all N keys -- the
+    rows of unsharded attention that the USP path must equal -- timed on
+    ``cores`` single-threaded spawn workers (rows split evenly), and once
+    more on one worker for a single-thread figure.  Parity: the same rows of
+    the step's fused output, already on the device."""
+    import numpy as np
+    from oracle import pool
+    glob = {n: wl.from_token_stack(step.host[n])[0, heads].float().numpy() for n in ("q", "k", "v")}
+    rows = wl.sample_rows(w, nrows).numpy()
+    jobs = pool.split_row_jobs(glob["q"], glob["k"], glob["v"], rows, w.scale, cores)
+    with pool.rows_executor(min(cores, len(jobs))) as ex:
+        t0 = time.perf_counter()
+        res = list(ex.map(pool.rows_job, jobs))
+        dt = time.perf_counter() - t0
+    ro, rl = pool.join_row_results(res, len(heads))
+    flop = 4.0 * len(heads) * len(rows) * w.N * w.D
+    # single thread: one worker, the first 2048 rows of the first head
+    one = pool.split_row_jobs(glob["q"][:1], glob["k"][:1], glob["v"][:1], rows[:2048], w.scale, 1)
+    with pool.rows_executor(1) as ex:
+        t1 = time.perf_counter()
+        list(ex.map(pool.rows_job, one))
+        dt1 = time.perf_counter() - t1
+    flop1 = 4.0 * min(2048, len(rows)) * w.N * w.D
+    sel = step.out_f[:, :, :, heads]
+    go = wl.from_token_stack(sel)[0][:, torch.as_tensor(rows, device=sel.device)].double().cpu().numpy()
+    gl = wl.from_token_stack(step.lse_f[:, :, :, heads])[0][:, torch.as_tensor(rows, device=sel.device)]
+    gl = gl.double().cpu().numpy()
+    parity = {"max_abs_out": float(np.abs(go - ro).max()),
+              "max_rel_lse": float((np.abs(gl - rl) / np.maximum(np.abs(rl), 1e-30)).max()),
+              "vs": f"oracle (numpy fp64) at the same {len(rows)} rows x {len(heads)} heads, the step's fused call",
+              "bound": {"out_abs": 2e-2, "lse_rel": 1e-3}}
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": min(cores, len(jobs)), "kind": "oracle",
+            "sample": (f"oracle attention (numpy fp64) of {len(rows)} seeded query rows of heads {list(heads)} of "
+                       f"{w.name} against all {w.N} keys, {dt:.1f} s (a rate over a bounded sample: nothing is "
+                       f"extrapolated)"),
+            "single_thread": {"value": flop1 / dt1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                              "sample": f"{min(2048, len(rows))} rows of head {heads[0]} on one worker, {dt1:.1f} s"},
+            "parity": parity}
+
+
+def oracle_single_thread(w, heads):
+    """The single-thread figure of the full-head CPU-baseline leg: one head
+    of the same sub-problem's attention on one single-threaded worker."""
+    import numpy as np
+    from oracle import pool
+    sub = wl.custom(w.name, w.dtype, w.B, w.ulysses, w.N, w.D, w.ulysses, w.ring, seed=w.seed, Nt=w.Nt)
+    inp = wl.make_inputs(sub, with_dout=False)
+    q, k, v = (inp[n][0, :1].float().numpy() for n in ("q", "k", "v"))
+    rows = np.arange(min(w.N, 1024))
+    one = pool.split_row_jobs(q, k, v, rows, w.scale, 1)
+    with pool.rows_executor(1) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(pool.rows_job, one))
+        dt = time.perf_counter() - t0
+    return {"value": 4.0 * len(rows) * w.N * w.D / dt / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "sample": f"{len(rows)} query rows of one head against all {w.N} keys on one worker, {dt:.2f} s"}
 
 
 def cpu_cores():
@@ -702,8 +765,7 @@ def our_arm(args, w, ws, rank, local):
         # The dQ kernel runs concurrently with dK/dV (launched second, its CTAs fill dK/dV's last
         # wave), so its event time (from the end of the prep to its own end) includes the time its
         # CTAs waited for SMs: it is reported, but only dK/dV (launched first, alone on the GPU until
-        # its tail) and the fused forward are roofline candidates.  Dominance by serialised device
-        # time: profiles/launches_qwen1024_step.md.
+        # its tail) and the fused forward are roofline candidates.
         kernels["usp_bwd_dkdv_kernel"] = (dkdv_s, 0.8 * w.bwd_flop, "backward dK/dV (S^T, dP^T, dV, dK GEMMs)")
         overlapped["usp_bwd_dq_kernel_overlapped_ms"] = dq_s * 1e3
     dom = max(kernels, key=lambda k: kernels[k][0])
@@ -711,6 +773,9 @@ def our_arm(args, w, ws, rank, local):
     ach = f_dom / t_dom / 1e12
     roofline = {"kernel": f"{dom}: {desc}", "bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "traffic": kernel_traffic(dom, w.name),
+                "traffic_source": ("profiles/traffic.json: dram__bytes_read.sum + dram__bytes_write.sum per launch "
+                                   "from one ncu capture, valid while the kernel source hash recorded there "
+                                   "matches (null otherwise)"),
                 "launch_ms": t_dom * 1e3, "algorithmic_flop_per_launch": f_dom,
                 "peak_kind": f"bf16 dense burst, {peaks['source']} (sustained {peaks['bf16_tflops_sustained']})"}
     for k, r in rows.items():
@@ -719,10 +784,16 @@ def our_arm(args, w, ws, rank, local):
     cpu = None
     if not args.no_cpu_baseline and ws == 1:   # the oracle baseline is taken on rank 0 of a 1-GPU run only
         heads = sample_heads(w)
-        dt, parity = run_oracle_sample(w, heads)
-        cpu = {"value": oracle_sample_flop(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
-               "kind": "oracle", "sample": f"oracle USP forward (numpy fp64) on {heads} of {w.H} heads, full N, "
-                                           f"{dt:.1f} s", "parity": parity}
+        if oracle_sample_flop(w, heads) <= 0.5e12:
+            dt, parity = run_oracle_sample(w, heads)
+            cpu = {"value": oracle_sample_flop(w, heads) / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(),
+                   "kind": "oracle", "sample": f"oracle USP forward (numpy fp64) on {heads} of {w.H} heads, full N, "
+                                               f"{dt:.1f} s", "parity": parity,
+                   "single_thread": oracle_single_thread(w, heads)}
+        elif not step.joint:
+            # heads on either side of a Ulysses head-group boundary, and the last head
+            hs = sorted({0, w.Hu - 1, w.Hu, w.H - 1})
+            cpu = oracle_rows_baseline(w, step, hs, 12288, cpu_cores())
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -768,10 +839,11 @@ def _lib_check(rc):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about ten seconds of work: 400 for the 1024^2 workloads, 20 for Wan 720p)")
+    ap.add_argument("--warmup", type=int, default=None, help="untimed warm-up steps (default 10, 3 for the Wan workloads)")
     ap.add_argument("--impl", default="usp", choices=["usp", "reference"])
-    ap.add_argument("--workload", default="qwen1024", choices=wl.ORDER + wl.JOINT)
+    ap.add_argument("--workload", default="wan720p", choices=wl.ORDER + wl.JOINT)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row GB/s timings")
@@ -781,6 +853,11 @@ def main():
     args = ap.parse_args()
     ws, rank, local = dist_env()
     w = wl.WORKLOADS[args.workload]
+    big = w.N * w.N * w.H > 1e11
+    if args.steps is None:
+        args.steps = 20 if big else 400
+    if args.warmup is None:
+        args.warmup = 3 if big else 10
     if args.impl == "reference":
         reference_arm(args, w, ws, rank)
         return

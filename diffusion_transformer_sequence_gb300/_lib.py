@@ -59,6 +59,7 @@ SIGNATURES = {
     "usp_device_status": (_int, [_vp]),
     "usp_status_string": (ctypes.c_char_p, [_int]),
     "usp_last_cuda_error": (_int, []),
+    "usp_set_debug_spin_limit": (None, [ctypes.c_longlong]),
     "usp_set_spin_limit": (None, [ctypes.c_longlong]),
     "usp_profile_phases": (_int, [_int]),
     "usp_profile_read": (_int, [ctypes.POINTER(ctypes.c_float), _int]),

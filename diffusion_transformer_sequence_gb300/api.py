@@ -300,4 +300,6 @@ def device_status() -> int:
 
 
 def set_spin_limit(polls: int) -> None:
-    _lib.lib().usp_set_spin_limit(int(polls))
+    """Test hook: polls a device-side wait may make before it gives up
+    (usp_set_debug_spin_limit; negative restores the default)."""
+    _lib.lib().usp_set_debug_spin_limit(int(polls))

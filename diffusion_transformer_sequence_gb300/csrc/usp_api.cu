@@ -39,6 +39,10 @@ struct PhaseState {
 thread_local PhaseState t_phase;
 
 }  // namespace
+int record_cuda_error(cudaError_t e) {
+  t_last_cuda_error = (int)e;
+  return USP_ERR_CUDA;
+}
 int phase_mark(cudaStream_t s, int from) {
   if (!t_phase.enabled || t_phase.marks == 0 || t_phase.marks > kMaxPhases) return -1;
   const int i = t_phase.marks;
@@ -61,10 +65,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 unsigned int* g_err_ptr[kMaxDevices] = {};
 
-int cuda_fail(cudaError_t e) {
-  t_last_cuda_error = (int)e;
-  return USP_ERR_CUDA;
-}
+int cuda_fail(cudaError_t e) { return record_cuda_error(e); }
 
 int err_word(unsigned int** out) {
   int dev = 0;
@@ -842,7 +843,9 @@ const char* usp_status_string(int status) {
 
 int usp_last_cuda_error(void) { return t_last_cuda_error; }
 
-void usp_set_spin_limit(long long polls) { g_spin_limit.store(polls < 0 ? -1 : polls); }
+void usp_set_debug_spin_limit(long long polls) { g_spin_limit.store(polls < 0 ? -1 : polls); }
+
+void usp_set_spin_limit(long long polls) { usp_set_debug_spin_limit(polls); }
 
 int usp_profile_phases(int enable) {
   if (enable && !t_phase.created) {

@@ -222,6 +222,9 @@ cudaError_t launch_attn_f32_bwd(const float* q, const float* k, const float* v, 
 // from event `from` (an earlier mark's return value; -1 = the previous mark)
 // to this one.  Returns this mark's index, or -1.
 int phase_mark(cudaStream_t s, int from = -1);
+// Remembers `e` as this thread's last CUDA error (usp_last_cuda_error) and
+// returns USP_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
 
 // Fork / join of the device's side stream: side_begin makes the side stream
 // wait for the work enqueued so far on `main` and hands it out (holding the

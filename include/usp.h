@@ -272,11 +272,14 @@ int usp_attention_fwd_fp8(const void* q, const void* k, const void* v, void* out
  * cudaMalloc/cudaFree (which may synchronise the device) on their request
  * path.  The pages have no counterpart to this call; it exists for such hosts.
  * Its scratch is one 64 MiB array compiled into the library (every device that
- * loads libusp holds it until exit).  Problems whose workspace
- * (usp_attention_workspace_bytes) exceeds 64 MiB return USP_ERR_WORKSPACE.
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the array and it keeps the last call's
+ * loads libusp holds it until exit).  Arguments are checked as
+ * usp_attention_fwd checks them, in the same order; a valid problem whose
+ * workspace (usp_attention_workspace_bytes) exceeds 64 MiB then returns
+ * USP_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current and caches it with
+ * the context's id; make that first call before any stream capture.  After a
+ * cudaDeviceReset the next call on that device looks the address up again
+ * (so that call, too, belongs outside a capture).  All calls share the array and it keeps the last call's
  * contents (nothing here needs it zeroed); calls that overlap on the GPU --
  * other streams or host threads -- race on it and must be serialised by the
  * caller.  Allocates nothing. */
@@ -327,7 +330,11 @@ int usp_last_cuda_error(void);
 
 /* Test hook: the number of polls a device-side wait may make before it
  * gives up (negative restores the default).  0 makes every wait that is not
- * already satisfied expire, so the timeout path runs without any hang. */
+ * already satisfied expire, so the timeout path runs without any hang.
+ * Applies to launches enqueued after the call, on every device. */
+void usp_set_debug_spin_limit(long long polls);
+
+/* The same hook under its earlier name (kept for existing callers). */
 void usp_set_spin_limit(long long polls);
 
 #ifdef __cplusplus

@@ -61,13 +61,42 @@ def sampled_attention(q, k, v, rows, scale, workers: int | None = None):
     workers = workers or default_workers()
     BH = q.shape[0]
     rows = np.asarray(rows, dtype=np.int64)
-    jobs = [(q[h][rows], k[h], v[h], np.arange(len(rows)), scale) for h in range(BH)]
+    jobs = split_row_jobs(q, k, v, rows, scale, workers)
     if workers == 1:
         res = [_rows_job(j) for j in jobs]
     else:
-        with _executor(min(workers, BH)) as ex:
+        with _executor(min(workers, len(jobs))) as ex:
             res = list(ex.map(_rows_job, jobs))
-    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])
+    return join_row_results(res, BH)
+
+
+def split_row_jobs(q, k, v, rows, scale, workers: int):
+    """One job per (head, slice of ``rows``): the rows of a head are cut into
+    as many slices as it takes to give every worker a job (rows are
+    independent, so this changes no arithmetic)."""
+    BH = q.shape[0]
+    rows = np.asarray(rows, dtype=np.int64)
+    per_head = max(1, min(len(rows), -(-workers // BH)))
+    cuts = np.array_split(np.arange(len(rows)), per_head)
+    return [(q[h][rows[c]], k[h], v[h], np.arange(len(c)), scale) for h in range(BH) for c in cuts if len(c)]
+
+
+def join_row_results(res, BH: int):
+    """Reassemble the per-(head, slice) results of :func:`split_row_jobs`."""
+    per = len(res) // BH
+    O = [np.concatenate([r[0] for r in res[h * per:(h + 1) * per]]) for h in range(BH)]
+    L = [np.concatenate([r[1] for r in res[h * per:(h + 1) * per]]) for h in range(BH)]
+    return np.stack(O), np.stack(L)
+
+
+def rows_executor(workers: int):
+    """A spawn pool of ``workers`` single-threaded oracle workers, started."""
+    return _executor(workers, 1)
+
+
+def rows_job(job):
+    """Run one job of :func:`split_row_jobs` (in a worker or in-process)."""
+    return _rows_job(job)
 
 
 def sampled_backward(q, k, v, dout, scale, heads, qrows, krows, workers: int | None = None):

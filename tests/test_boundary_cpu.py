@@ -26,6 +26,17 @@ def test_exports_every_declared_symbol(L):
     assert set(declared) == set(_lib.SIGNATURES), "binding signatures out of sync with usp.h"
 
 
+def test_boundary_names_of_the_scope_table(L):
+    """The C ABI carries every entry point the hot path's scope names,
+    including the bounded-wait test hook under its listed name (the earlier
+    name stays as an alias)."""
+    for name in ("usp_relayout_tok2head", "usp_relayout_head2tok", "usp_attn_chunk_fwd", "usp_lse_merge",
+                 "usp_attention_workspace_bytes", "usp_attention_fwd", "usp_attention_bwd",
+                 "usp_status_string", "usp_last_cuda_error", "usp_set_debug_spin_limit", "usp_set_spin_limit"):
+        assert hasattr(L, name), name
+    L.usp_set_debug_spin_limit(-1)   # host-side only: restores the default poll limit
+
+
 def _header_prototypes():
     """name -> list of (C type of each parameter) parsed from include/usp.h."""
     import re

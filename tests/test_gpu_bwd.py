@@ -179,6 +179,46 @@ def test_bwd_qwen_workloads_sampled(name, heads):
         _check_grad(sel(dv, krows), r_dv, "bf16", f"{name} {mode} dv")
 
 
+# (B, H, N, ulysses, ring): Qwen-Image 2048^2 (u4, Ns = 4096), a u8 grid with
+# Ns = 256, and a hybrid u2 x r2 grid with Ns = 512.  Every shard is a whole
+# number of 128-row tiles.
+BITWISE = [(1, 24, 16384, 4, 1), (1, 8, 2048, 8, 1), (2, 4, 2048, 2, 2)]
+
+
+@pytest.mark.parametrize("B,H,N,u,r", BITWISE)
+def test_bwd_sharded_bitwise_equals_unsharded(B, H, N, u, r):
+    """The USP PR page (Validation, Numerics) finds Ulysses-only USP equal to
+    sp = 1 bit for bit, the input gradients included: the exchange only moves
+    data.  Here both backward calls over the sharded stacks, given the same
+    forward out and lse, must equal the unsharded (u = r = 1) backward bit for
+    bit.  This holds when every shard is a whole number of 128-row tiles: the
+    kernels then see the same global tiles in the same order whatever the
+    grid.  (With a ragged shard the last tile of each shard is short, the
+    per-tile partial sums are grouped differently and results agree to
+    rounding only; the small-problem tests above check those grids against
+    the oracle.)  The hybrid u x r case checks the same for the backward
+    alone: its forward merges ring partials and is not bitwise sp = 1, so
+    the test feeds both calls one out and lse."""
+    usp = _usp()
+    w = wl.custom("bwdbit", "bf16", B, H, N, 128, u, r, seed=31, backward=True)
+    assert w.Ns % 128 == 0
+    g = {n: t.cuda() for n, t in wl.make_inputs(w, with_dout=True).items()}
+    one = {n: wl.to_token_stack(t, 1, 1) for n, t in g.items()}      # u = r = 1: the plain layout
+    o, l = usp.attention_fwd(one["q"], one["k"], one["v"], 1, 1, w.scale, mode="fused")
+    ref = [wl.from_token_stack(t) for t in
+           usp.attention_bwd(one["q"], one["k"], one["v"], o, l, one["dout"], 1, 1, w.scale, mode="fused")]
+    st = {n: wl.to_token_stack(t, u, r) for n, t in g.items()}
+    so, sl = wl.to_token_stack(wl.from_token_stack(o), u, r), wl.to_token_stack(wl.from_token_stack(l), u, r)
+    for mode in ("fused", "materialised"):
+        got = usp.attention_bwd(st["q"], st["k"], st["v"], so, sl, st["dout"], u, r, w.scale, mode=mode)
+        assert usp.device_status() == 0
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            a = wl.from_token_stack(a)
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
+                f"{mode} u{u} r{r}: {name} differs from the unsharded backward " \
+                f"({int((a != b).sum())} elements, max |diff| {float((a.float() - b.float()).abs().max()):.3e})"
+
+
 def _small_bwd_inputs(seed=21):
     w = wl.custom("bwdc", "bf16", 1, 4, 1024, 128, 2, 2, seed=seed, backward=True)
     inp = wl.make_inputs(w)
