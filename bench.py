@@ -340,12 +340,12 @@ class Step:
             usp.attention_fwd(self.dev["q"], self.dev["k"], self.dev["v"], w.ulysses, w.ring, w.scale,
                               mode="fused", out=self.out_f, lse=self.lse_f)
         self.flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-        # materialised: tok2head (q, k, v in one launch), chunk attention, merge (ring > 1), head2tok of out
-        # and lse (one launch when both move in 16-byte vectors, else two); fused: one; backward: prep +
-        # dK/dV + dQ
+        # materialised: tok2head (q, k, v in one launch), chunk attention, then the merge into the
+        # token-sharded out and lse (ring > 1, one launch) or head2tok of out and lse (ring = 1: one launch
+        # when both move in 16-byte vectors, else two); fused: one; backward: prep + dK/dV + dQ
         elt = 2 if w.dtype == "bf16" else 4
         h2t = 1 if (w.Ns * 4) % 16 == 0 and (w.Ns * w.D * elt) % 16 == 0 else 2
-        self.launches_per_step = 2 + (1 if w.ring > 1 else 0) + h2t + 1 + (3 if backward else 0)
+        self.launches_per_step = 2 + (1 if w.ring > 1 else h2t) + 1 + (3 if backward else 0)
         self.joint = w.Nt > 0
         if self.joint:
             # text tokens replicated on every virtual rank: q_txt, k_txt, v_txt [B, H, Nt, D]
@@ -359,8 +359,8 @@ class Step:
                                             "materialised", True)
             self.ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
             # materialised: tok2head, partials against the image chunks, partials against the text,
-            # merge, head2tok of out and lse, text merge; fused: one launch (image and text queries)
-            self.launches_per_step = 5 + h2t + 1
+            # merge into the token-sharded out and lse, text merge; fused: one launch (image and text queries)
+            self.launches_per_step = 5 + 1
 
     def flop(self):
         if self.joint:
@@ -572,7 +572,8 @@ def time_rows(w, reps=10):
     res["head2tok"] = {"GB/s": 2 * w.t_bytes / t / 1e9, "us": t * 1e6, "bytes": 2 * w.t_bytes}
     if w.dtype == "bf16":
         # the bandwidth-bound launches inside the materialised forward, as the step runs them:
-        # tok2head of q, k, v in one launch, the ring merge, head2tok of out and lse (phase events)
+        # tok2head of q, k, v in one launch, then the ring merge written straight to the token-sharded
+        # out and lse (ring > 1) or head2tok of out and lse (ring = 1) (phase events)
         import ctypes
         L = usp.lib()
         kk, vv = torch.randn_like(q), torch.randn_like(q)
@@ -593,13 +594,15 @@ def time_rows(w, reps=10):
         lse_b = w.B * w.H * w.N * 4
         t_in = statistics.median(p_[0] for p_ in ph)
         res["tok2head_qkv_in_step"] = {"GB/s": 6 * w.t_bytes / t_in / 1e9, "us": t_in * 1e6, "bytes": 6 * w.t_bytes}
+        t_out = statistics.median(p_[2] for p_ in ph)
         if w.ring > 1:
-            t_m = statistics.median(p_[2] for p_ in ph)
+            # the ring merge writes the token-sharded out and lse directly (merge + head2tok, one launch):
+            # reads ring partial planes and their lse, writes one plane and one lse
             byt = (w.ring + 1) * (w.t_bytes + lse_b)
-            res["lse_merge_in_step"] = {"GB/s": byt / t_m / 1e9, "us": t_m * 1e6, "bytes": byt}
-        t_out = statistics.median(p_[3] for p_ in ph)
-        byt = 2 * (w.t_bytes + lse_b)
-        res["head2tok_out_lse_in_step"] = {"GB/s": byt / t_out / 1e9, "us": t_out * 1e6, "bytes": byt}
+            res["merge_head2tok_in_step"] = {"GB/s": byt / t_out / 1e9, "us": t_out * 1e6, "bytes": byt}
+        else:
+            byt = 2 * (w.t_bytes + lse_b)
+            res["head2tok_out_lse_in_step"] = {"GB/s": byt / t_out / 1e9, "us": t_out * 1e6, "bytes": byt}
     if w.dtype == "bf16" and not w.Nt:
         # the backward through the materialised Ulysses path (tok2head of q, k, v, O, dO and lse,
         # the per-rank chunk backward over the head-sharded stacks, head2tok of dq, dk, dv),

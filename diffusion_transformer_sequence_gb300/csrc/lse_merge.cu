@@ -8,13 +8,22 @@
 // The merge is over the R ring steps of one row, not across D, so a row's D
 // elements are split over threads in 16-byte vectors and no cross-thread
 // reduction is needed.  HBM-bound: reads R rows of partials + R LSEs, writes
-// one row + one LSE.
+// one row + one LSE.  Inside the materialised USP forward the merge also
+// performs the Ulysses head -> token re-layout (merge_tok_kernel).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
 #include "usp_internal.cuh"
 
 namespace usp {
+
+bool lse_merge_to_tokens_ok(const void* outs, const void* out, int R, int64_t B, int64_t Hu, int64_t Nr, int64_t D,
+                            int u, int r) {
+  const uintptr_t a = (uintptr_t)outs | (uintptr_t)out;
+  return (D == 128 || D == 64 || D == 32 || D == 16) && (a & 15) == 0 && R >= 1 && R <= 8 &&
+         B * Hu <= 65535 && (int64_t)r * u <= 65535 && Nr * 16 + 255 < 2147483647LL;
+}
+
 namespace {
 
 __device__ __forceinline__ void store8(__nv_bfloat16* p, const float* f) {
@@ -137,6 +146,135 @@ __global__ void __launch_bounds__(256) merge_scalar_kernel(const T* __restrict__
   if (gt - row * D == 0) lse[row] = L;
 }
 
+// The merge fused with the Ulysses head -> token re-layout: the partials are
+// planes of the head-sharded stack [r, u, B, Hu, Nr, D]; each merged row
+// goes straight to its place in the token-sharded stack [r, u, B, H, Ns, D]
+// (and its LSE to [r, u, B, H, Ns]), so the merged head-sharded result is
+// never written.  Head-sharded row (g, j, b, h', n) is token-sharded row
+// (g, n / Ns, b, j*Hu + h', n % Ns): the handbook's all_to_all_tokens as
+// addressing.  grid.z = g*u + j, grid.y = b*Hu + h', grid.x = blocks of
+// rows; a thread merges kVec 8-element vectors of one row (D / (8*kVec)
+// threads per row), so the index arithmetic is paid once per 8*kVec elements.
+template <typename T, int kMaxR, int kD, int kVec>
+__global__ void __launch_bounds__(256) merge_tok_kernel(const T* __restrict__ outs, const float* __restrict__ lses,
+                                                        int R, T* __restrict__ out, float* __restrict__ lse,
+                                                        int64_t rows, int u, int B, int Hu, int Nr, int Ns) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
+  constexpr int kTpr = kD / (8 * kVec);  // threads per row
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int n = t / kTpr;
+  if (n >= Nr) return;
+  const int c0 = (t - n * kTpr) * 8;
+  const int j = (int)blockIdx.z % u, g = (int)blockIdx.z / u;
+  const int b = (int)blockIdx.y / Hu, hh = (int)blockIdx.y - b * Hu;
+  const int s = n / Ns, n2 = n - s * Ns;
+  const int64_t unit = ((int64_t)blockIdx.z * B + b) * Hu + hh;
+  const int64_t row = unit * Nr + n;
+  const int64_t orow = ((((int64_t)g * u + s) * B + b) * ((int64_t)u * Hu) + (int64_t)j * Hu + hh) * Ns + n2;
+  const int64_t plane = rows * kD;
+  Raw8<T> x[kMaxR][kVec];
+  float lv[kMaxR];
+#pragma unroll
+  for (int q = 0; q < kMaxR; ++q) {
+    if (q < R) {
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) x[q][v].load(outs + q * plane + row * kD + c0 + v * 8 * kTpr);
+      lv[q] = __ldg(lses + q * rows + row);
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kMaxR; ++q)
+    if (q < R) m = fmaxf(m, lv[q]);
+  float sum = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMaxR; ++q)
+    if (q < R) sum += __expf(lv[q] - m);
+  const float L = m + __logf(sum);
+  float wt[kMaxR];
+#pragma unroll
+  for (int q = 0; q < kMaxR; ++q) wt[q] = q < R ? __expf(lv[q] - L) : 0.f;
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int q = 0; q < kMaxR; ++q) {
+      if (q < R) {
+        float f[8];
+        x[q][v].get(f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wt[q], f[i], acc[i]);
+      }
+    }
+    store8(out + orow * kD + c0 + v * 8 * kTpr, acc);
+  }
+  if (c0 == 0) lse[orow] = L;
+}
+
+// Generic form of merge_tok_kernel: one thread per output element.
+template <typename T>
+__global__ void __launch_bounds__(256) merge_tok_scalar_kernel(const T* __restrict__ outs,
+                                                               const float* __restrict__ lses, int R,
+                                                               T* __restrict__ out, float* __restrict__ lse,
+                                                               int64_t rows, int64_t D, int64_t u, int64_t B,
+                                                               int64_t Hu, int64_t Nr, int64_t Ns) {
+  ptx::griddep_wait();
+  ptx::griddep_launch();
+  const int64_t gt = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gt >= rows * D) return;
+  const int64_t row = gt / D, d = gt - row * D;
+  const int64_t unit = row / Nr, n = row - unit * Nr;
+  const int64_t hh = unit % Hu, b = (unit / Hu) % B, j = (unit / Hu / B) % u, g = unit / Hu / B / u;
+  const int64_t s = n / Ns;
+  const int64_t orow = (((g * u + s) * B + b) * (u * Hu) + j * Hu + hh) * Ns + (n - s * Ns);
+  float m = -INFINITY;
+  for (int q = 0; q < R; ++q) m = fmaxf(m, lses[q * rows + row]);
+  float sum = 0.f;
+  for (int q = 0; q < R; ++q) sum += expf(lses[q * rows + row] - m);
+  const float L = m + logf(sum);
+  float acc = 0.f;
+  for (int q = 0; q < R; ++q) acc = fmaf(expf(lses[q * rows + row] - L), to_f(outs[q * rows * D + gt]), acc);
+  from_f(out + orow * D + d, acc);
+  if (d == 0) lse[orow] = L;
+}
+
+template <typename T, int kD, int kVec>
+cudaError_t launch_tok_vec(const void* outs, const float* lses, int R, void* out, float* lse, int64_t rows, int u,
+                           int B, int Hu, int Nr, int Ns, int r, cudaStream_t stream) {
+  constexpr int kTpr = kD / (8 * kVec);
+  const dim3 g((unsigned)(((int64_t)Nr * kTpr + 255) / 256), (unsigned)(B * Hu), (unsigned)(r * u)), b(256);
+  if (R <= 2)
+    return launch_pdl(merge_tok_kernel<T, 2, kD, kVec>, g, b, 0, stream, (const T*)outs, lses, R, (T*)out, lse, rows,
+                      u, B, Hu, Nr, Ns);
+  if (R <= 4)
+    return launch_pdl(merge_tok_kernel<T, 4, kD, kVec>, g, b, 0, stream, (const T*)outs, lses, R, (T*)out, lse, rows,
+                      u, B, Hu, Nr, Ns);
+  return launch_pdl(merge_tok_kernel<T, 8, kD, kVec>, g, b, 0, stream, (const T*)outs, lses, R, (T*)out, lse, rows, u,
+                    B, Hu, Nr, Ns);
+}
+
+template <typename T>
+cudaError_t launch_typed_tok(const void* outs, const float* lses, int R, void* out, float* lse, int64_t B,
+                             int64_t Hu, int64_t Nr, int64_t D, int u, int r, cudaStream_t stream) {
+  const int64_t Ns = Nr / u;
+  const int64_t rows = (int64_t)r * u * B * Hu * Nr;
+  if (lse_merge_to_tokens_ok(outs, out, R, B, Hu, Nr, D, u, r)) {
+    const int iu = u, iB = (int)B, iHu = (int)Hu, iNr = (int)Nr, iNs = (int)Ns;
+    // four vectors per thread for bf16 (64 bytes of each partial), two for fp32
+    if (D == 128 && sizeof(T) == 2)
+      return launch_tok_vec<T, 128, 4>(outs, lses, R, out, lse, rows, iu, iB, iHu, iNr, iNs, r, stream);
+    if (D == 128) return launch_tok_vec<T, 128, 2>(outs, lses, R, out, lse, rows, iu, iB, iHu, iNr, iNs, r, stream);
+    if (D == 64) return launch_tok_vec<T, 64, 2>(outs, lses, R, out, lse, rows, iu, iB, iHu, iNr, iNs, r, stream);
+    if (D == 32) return launch_tok_vec<T, 32, 2>(outs, lses, R, out, lse, rows, iu, iB, iHu, iNr, iNs, r, stream);
+    if (D == 16) return launch_tok_vec<T, 16, 1>(outs, lses, R, out, lse, rows, iu, iB, iHu, iNr, iNs, r, stream);
+  }
+  return launch_pdl(merge_tok_scalar_kernel<T>, dim3((unsigned)((rows * D + 255) / 256)), dim3(256), 0, stream,
+                    (const T*)outs, lses, R, (T*)out, lse, rows, D, (int64_t)u, B, Hu, Nr, Ns);
+}
+
 template <typename T>
 cudaError_t launch_typed(const void* outs, const float* lses, int R, void* out, float* lse, int64_t rows,
                          int64_t D, cudaStream_t stream) {
@@ -156,6 +294,13 @@ cudaError_t launch_typed(const void* outs, const float* lses, int R, void* out, 
 }
 
 }  // namespace
+
+cudaError_t launch_lse_merge_to_tokens(const void* outs, const float* lses, int R, void* out, float* lse, int64_t B,
+                                       int64_t Hu, int64_t Nr, int64_t D, int u, int r, int dtype,
+                                       cudaStream_t stream) {
+  if (dtype == 1) return launch_typed_tok<__nv_bfloat16>(outs, lses, R, out, lse, B, Hu, Nr, D, u, r, stream);
+  return launch_typed_tok<float>(outs, lses, R, out, lse, B, Hu, Nr, D, u, r, stream);
+}
 
 cudaError_t launch_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
                              int64_t rows, int64_t D, int dtype, cudaStream_t stream) {

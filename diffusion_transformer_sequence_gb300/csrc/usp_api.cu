@@ -169,12 +169,13 @@ FwdWorkspace fwd_layout(int64_t B, int64_t H, int64_t N, int64_t D, int r, usp_d
   w.xq = off; off += t;
   w.xk = off; off += t;
   w.xv = off; off += t;
-  if (r > 1) {
+  if (r > 1) {  // the merge writes the token-sharded result directly
     w.parts_o = off; off += (size_t)r * t;
     w.parts_l = off; off += (size_t)r * lb;
+  } else {       // the chunk result, re-laid out head -> token afterwards
+    w.xo = off; off += t;
+    w.xl = off; off += lb;
   }
-  w.xo = off; off += t;
-  w.xl = off; off += lb;
   w.total = off;
   return w;
 }
@@ -183,7 +184,7 @@ FwdWorkspace fwd_layout(int64_t B, int64_t H, int64_t N, int64_t D, int r, usp_d
 // with ring + 1 partial planes (the last against the text K/V), plus the
 // text-query partials (ring chunk planes + one text plane) when requested.
 struct JointWorkspace {
-  size_t xq, xk, xv, parts_o, parts_l, xo, xl, tparts_o, tparts_l, total;
+  size_t xq, xk, xv, parts_o, parts_l, tparts_o, tparts_l, total;
 };
 JointWorkspace joint_layout(int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t D, int r, usp_dtype dt,
                             bool text_queries) {
@@ -194,10 +195,8 @@ JointWorkspace joint_layout(int64_t B, int64_t H, int64_t N, int64_t Nt, int64_t
   w.xq = off; off += t;
   w.xk = off; off += t;
   w.xv = off; off += t;
-  w.parts_o = off; off += (size_t)(r + 1) * t;
+  w.parts_o = off; off += (size_t)(r + 1) * t;  // merged straight into the token-sharded out, lse
   w.parts_l = off; off += (size_t)(r + 1) * lb;
-  w.xo = off; off += t;
-  w.xl = off; off += lb;
   if (text_queries) {
     w.tparts_o = off; off += (size_t)(r + 1) * round_up((size_t)(B * H * Nt * D) * elt_size(dt));
     w.tparts_l = off; off += (size_t)(r + 1) * round_up((size_t)(B * H * Nt) * 4);
@@ -445,13 +444,13 @@ int usp_attention_fwd(const void* q, const void* k, const void* v, void* out, fl
       USP_OK)
     return st;
   phase_mark(s);
-  if (r > 1) {
-    cudaError_t e = launch_lse_merge(ws + w.parts_o, (const float*)(ws + w.parts_l), r, ws + w.xo,
-                                     (float*)(ws + w.xl), B * H * N, D, (int)dtype, s);
+  if (r > 1) {  // ring merge and the Ulysses head -> token exchange in one pass
+    cudaError_t e = launch_lse_merge_to_tokens(ws + w.parts_o, (const float*)(ws + w.parts_l), r, out, lse, B, Hu,
+                                               Nr, D, u, r, (int)dtype, s);
     if (e != cudaSuccess) return cuda_fail(e);
+  } else {
+    st = relayout_with_lse(ws + w.xo, out, (const float*)(ws + w.xl), lse, B, H, N, D, u, r, elt, false, s);
   }
-  phase_mark(s);
-  st = relayout_with_lse(ws + w.xo, out, (const float*)(ws + w.xl), lse, B, H, N, D, u, r, elt, false, s);
   phase_mark(s);
   return st;
 }
@@ -592,14 +591,10 @@ int usp_attention_fwd_joint(const void* q, const void* k, const void* v, const v
     if (st != USP_OK) return st;
   }
   if (prof) phase_mark(s);
-  if (N > 0) {
-    cudaError_t e = launch_lse_merge(ws + w.parts_o, (const float*)(ws + w.parts_l), r + 1, ws + w.xo,
-                                     (float*)(ws + w.xl), BH * N, D, (int)dtype, s);
+  if (N > 0) {  // ring + text merge and the Ulysses head -> token exchange in one pass
+    cudaError_t e = launch_lse_merge_to_tokens(ws + w.parts_o, (const float*)(ws + w.parts_l), (int)(r + 1), out, lse,
+                                               B, Hu, Nr, D, u, r, (int)dtype, s);
     if (e != cudaSuccess) return cuda_fail(e);
-    if (prof) phase_mark(s);
-    if ((st = relayout_with_lse(ws + w.xo, out, (const float*)(ws + w.xl), lse, B, H, N, D, u, r, elt, false, s)) !=
-        USP_OK)
-      return st;
     if (prof) phase_mark(s);
   }
   if (tq) {

@@ -88,6 +88,15 @@ cudaError_t launch_relayout_n(const void* const* srcs, void* const* dsts, int co
                               int64_t Ns, int64_t D, int ulysses, int ring, int elt, bool tok2head,
                               cudaStream_t stream);
 
+// The merge of R head-sharded partial planes [r, u, B, Hu, Nr, D] written
+// straight into the token-sharded stacks out [r, u, B, H, Ns, D] and lse
+// [r, u, B, H, Ns]; 16-byte vectors when lse_merge_to_tokens_ok (D % 8,
+// aligned pointers, R <= 8, 32-bit row indices), else one element per thread.
+bool lse_merge_to_tokens_ok(const void* outs, const void* out, int R, int64_t B, int64_t Hu, int64_t Nr, int64_t D,
+                            int u, int r);
+cudaError_t launch_lse_merge_to_tokens(const void* outs, const float* lses, int R, void* out, float* lse, int64_t B,
+                                       int64_t Hu, int64_t Nr, int64_t D, int u, int r, int dtype,
+                                       cudaStream_t stream);
 cudaError_t launch_lse_merge(const void* outs, const float* lses, int R, void* out, float* lse,
                              int64_t rows, int64_t D, int dtype, cudaStream_t stream);
 

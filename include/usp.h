@@ -136,7 +136,10 @@ size_t usp_attention_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D,
  * The result equals unsharded attention of the re-assembled sequence.
  *   USP_MATERIALISED: tok2head(q,k,v) -> for every rank (g, j) and ring step
  *     t the chunk attention against KV chunk (g - t) mod ring -> merge over
- *     t -> head2tok(out, lse).  Partial outputs are stored in `dtype`.
+ *     t -> head2tok(out, lse).  Partial outputs are stored in `dtype`.  With
+ *     ring > 1 the merge writes each merged row straight to its token-sharded
+ *     place (merge and head2tok in one pass); with ring = 1 the chunk result
+ *     is re-laid out head -> token.
  *     Needs usp_attention_workspace_bytes() of workspace.
  *   USP_FUSED: one kernel reads q, k, v in place and keeps the ring merge
  *     in registers (online softmax over every KV chunk); no workspace.
@@ -200,7 +203,8 @@ size_t usp_attention_joint_workspace_bytes(int64_t B, int64_t H, int64_t N, int6
  * every query over the Nt text + N image keys of its head.
  *   USP_MATERIALISED: tok2head(q,k,v) -> per rank (g, j) the ring chunk
  *     partials (as usp_attention_fwd) plus one partial against the text K/V
- *     of head group j -> merge of ring + 1 partials -> head2tok.  Text
+ *     of head group j -> merge of ring + 1 partials written straight to the
+ *     token-sharded out, lse (the merge and head2tok in one pass).  Text
  *     queries of head group j: one partial per ring chunk c of that group
  *     (the same on every ring rank, computed once) plus one against the
  *     text K/V -> merge into out_txt, lse_txt.  The launch of the partials
@@ -291,8 +295,10 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  * usp_attention_fwd / usp_attention_bwd call on this thread records a CUDA
  * event on its stream before its first kernel and after each kernel group:
  *   fused forward:        [attention]
- *   materialised forward: [tok2head q,k,v] [chunk attention] [merge]
- *                         [head2tok of out and lse (one launch when Ns % 4 == 0)]
+ *   materialised forward: [tok2head q,k,v] [chunk attention]
+ *                         [ring > 1: merge into the token-sharded out and lse |
+ *                          ring = 1: head2tok of out and lse (one launch when
+ *                          Ns % 4 == 0)]
  *   bf16 backward:        [Delta/lse prep] [dK,dV kernel] [dQ kernel]
  *                         (the two kernels run concurrently; both phases
  *                         are timed from the end of the prep)
@@ -302,8 +308,8 @@ int usp_attention_fwd_noalloc(const void* q, const void* k, const void* v, void*
  *   FP8 forward:          [quantise q, k, v] [FP8 attention]
  *   joint fused:          [attention: image and text queries, one launch]
  *   joint materialised:   [tok2head q,k,v] [partials against the image chunks
- *                         and against the text] [merge] [head2tok of out and lse]
- *                         [text-query merge]
+ *                         and against the text] [merge into the token-sharded
+ *                         out and lse] [text-query merge]
  * (the fp32 fused forward and usp_attention_bwd record nothing; the fp32
  * materialised backward records [tok2head] [backward] [head2tok]).  The events
  * are created by the library on first enable; enabling starts a fresh

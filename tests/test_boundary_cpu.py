@@ -138,7 +138,7 @@ def test_attention_validation_and_workspace(L):
     ws = L.usp_attention_workspace_bytes(1, 40, 32768, 128, 8, 4, 1, 0, 0)
     t = 40 * 32768 * 128 * 2
     lb = 40 * 32768 * 4
-    assert ws == 3 * t + 4 * t + 4 * lb + t + lb
+    assert ws == 3 * t + 4 * t + 4 * lb          # head-sharded q, k, v and the ring partials (merged into out)
     assert f(*a, 1, 40, 32768, 128, 8, 4, 0.1, 1, 0, FAKE, ws - 1, None) == 4
     assert L.usp_attention_workspace_bytes(1, 40, 32768, 128, 8, 4, 1, 1, 0) == 0   # fused: none
     assert L.usp_attention_workspace_bytes(1, 24, 16384, 128, 4, 1, 1, 0, 0) == 4 * 24 * 16384 * 128 * 2 + 24 * 16384 * 4
@@ -206,7 +206,7 @@ def test_joint_validation_and_workspace(L):
     t, lb = 24 * 4096 * 128 * 2, 24 * 4096 * 4
     tt, tlb = 24 * 512 * 128 * 2, 24 * 512 * 4
     ws = L.usp_attention_joint_workspace_bytes(1, 24, 4096, 512, 128, 2, 2, 1, 0, 1)
-    assert ws == 3 * t + 3 * t + 3 * lb + t + lb + 3 * tt + 3 * tlb
+    assert ws == 3 * t + 3 * t + 3 * lb + 3 * tt + 3 * tlb
     assert L.usp_attention_joint_workspace_bytes(1, 24, 4096, 512, 128, 2, 2, 1, 0, 0) == ws - 3 * tt - 3 * tlb
     assert f(*img, *txt, *outs, *base, 0, FAKE, ws - 1, None) == 4
     assert L.usp_attention_joint_workspace_bytes(1, 24, 4096, 512, 128, 2, 2, 1, 1, 1) == 0   # fused: none

@@ -44,15 +44,19 @@ def _noalloc(L, _lib, w, q, k, v):
 
 
 def _largest_fitting_bf16_n(L, _lib, H=8, u=2, r=2):
-    """The largest N (a multiple of u*r) whose materialised workspace still fits the array."""
+    """The largest N (a multiple of u*r) whose materialised workspace still fits the array
+    (found by bisection over the library's own workspace query)."""
     sp = u * r
-    n = (SCRATCH_BYTES // (H * 128 * 2 * 6)) // sp * sp + 8 * sp
-    while n > sp:
-        need = L.usp_attention_workspace_bytes(1, H, n, 128, u, r, _lib.USP_BF16, _lib.USP_MATERIALISED, 0)
-        if 0 < need <= SCRATCH_BYTES:
-            return n, need
-        n -= sp
-    raise AssertionError("no size fits")
+    need = lambda n: L.usp_attention_workspace_bytes(1, H, n * sp, 128, u, r, _lib.USP_BF16,
+                                                     _lib.USP_MATERIALISED, 0)
+    lo, hi = 1, 2
+    assert 0 < need(lo) <= SCRATCH_BYTES
+    while need(hi) <= SCRATCH_BYTES:
+        lo, hi = hi, 2 * hi
+    while hi - lo > 1:                       # need(lo) fits, need(hi) does not
+        mid = (lo + hi) // 2
+        lo, hi = (mid, hi) if need(mid) <= SCRATCH_BYTES else (lo, mid)
+    return lo * sp, need(lo)
 
 
 def _cases(L, _lib):
