@@ -859,11 +859,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row GB/s timings")
     ap.add_argument("--no-backward", action="store_true", help="leave usp_attention_bwd out of the step")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads (a multiple of its ulysses degree): a head-reduced "
+                         "case of the same per-head shape for profiling captures; not a bench line")
     ap.add_argument("--only", choices=["materialised", "fused", "backward"], default=None,
                     help="run one of the two forward calls per step (profiling)")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     w = wl.WORKLOADS[args.workload]
+    if args.heads is not None:
+        if args.heads < w.ulysses or args.heads % w.ulysses:
+            raise SystemExit(f"--heads must be a positive multiple of {w.ulysses}")
+        import dataclasses
+        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
     big = w.N * w.N * w.H > 1e11
     if args.steps is None:
         args.steps = 20 if big else 400
