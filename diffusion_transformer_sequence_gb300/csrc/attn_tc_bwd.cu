@@ -372,8 +372,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // streamed K through a 3-slot ring and V through a 2-slot ring (a K tile is
 // read by S(j) and, late, by dQ(j); a V tile only by dP(j), so the two are
 // released at different times and K needs the deeper ring to keep the next
-// loads in flight).
-// TMEM: S [0,128)  dP [128,256)  dQ [256,384)  dS buffers [384,448) [448,512).
+// loads in flight).  Q is also copied once into TMEM (bf16 pairs), so
+// S = Q K^T reads only K from shared memory: shared-memory bandwidth is what
+// the GEMMs of this kernel share with the K/V loads.
+// TMEM: S [0,128)  dP [128,256)  dQ [256,384)  dS [384,448)  Q [448,512).
 // =====================================================================
 constexpr int KSLOTS = 3, VSLOTS = 2;
 constexpr int DQ_OFF_K = 2 * TILE_BYTES;
@@ -389,9 +391,10 @@ enum DqBar : int {
   Q_DPFULL,
   Q_SFREE,                  // S(j) read by the warps (256 arrivals)
   Q_DPFREE,                 // dP(j) read (256)
-  Q_DSREADY,                // + dS buffer (256)
-  Q_DQDONE = Q_DSREADY + 2, // + dS buffer
-  Q_ODONE = Q_DQDONE + 2,
+  Q_DSREADY,                // dS(j) written (256)
+  Q_DQDONE,                 // dQ GEMM of tile j (which read dS(j)) done
+  Q_QTMEM,                  // Q copied into TMEM (256)
+  Q_ODONE,
   Q_MMADONE,
   Q_NUM_BARS
 };
@@ -428,10 +431,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::mbar_init(bar(Q_DPFULL), 1);
     ptx::mbar_init(bar(Q_SFREE), 256);
     ptx::mbar_init(bar(Q_DPFREE), 256);
-    for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(bar(Q_DSREADY + b), 256);
-      ptx::mbar_init(bar(Q_DQDONE + b), 1);
-    }
+    ptx::mbar_init(bar(Q_DSREADY), 256);
+    ptx::mbar_init(bar(Q_DQDONE), 1);
+    ptx::mbar_init(bar(Q_QTMEM), 256);
     ptx::mbar_init(bar(Q_ODONE), 1);
     ptx::mbar_init(bar(Q_MMADONE), 1);
     *abort_flag = 0;
@@ -446,7 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<uint32_t*>(smem + DQ_OFF_SLOT);
-  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdQ = tmem + 256, tdS = tmem + 384, tQ = tmem + 448;
   const int T = p.tiles;
 
   if (warp < 4) {
@@ -483,17 +485,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---------------------------------------------------------- MMA issuer
       constexpr uint32_t ID_S = ptx::idesc_bf16_f32(BM, BM, 0, 0);  // S, dP
       constexpr uint32_t ID_G = ptx::idesc_bf16_f32(BM, HD, 0, 1);  // dQ (B = K, N-major)
-      const uint64_t dQ0 = ptx::smem_desc_sw128(sbase + OFF_A0, 16, 1024);
       const uint64_t dO0 = ptx::smem_desc_sw128(sbase + OFF_A1, 16, 1024);
       auto wait = [&](int b, uint32_t ph) { return ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutMma); };
-      auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T
+      auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T (A = Q in TMEM)
         const int sk = j % KSLOTS;
         if (!wait(Q_KFULL + sk, (uint32_t)((j / KSLOTS) & 1))) return false;
         ptx::tc_fence_after();
         const uint64_t dk = ptx::launder(ptx::smem_desc_sw128(sbase + DQ_OFF_K + sk * TILE_BYTES, 16, 1024));
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          ptx::mma_ss(tS, kmajor_step(dQ0, kk), kmajor_step(dk, kk), ID_S, kk > 0 ? 1u : 0u);
+          ptx::mma_ts(tS, tQ + kk * 8, kmajor_step(dk, kk), ID_S, kk > 0 ? 1u : 0u);
         ptx::mma_commit(bar(Q_SFULL));
         return true;
       };
@@ -510,6 +511,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       bool ok = wait(Q_RES, 0);
+      if (ok) ok = wait(Q_QTMEM, 0);
       if (ok) ok = issue_s(0);
       if (ok) ok = issue_dp(0);
       for (int j = 0; ok && j < T; ++j) {
@@ -519,16 +521,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!(ok = wait(Q_DPFREE, (uint32_t)(j & 1)))) break;   // dP(j) read by the warps
           if (!(ok = issue_dp(j + 1))) break;
         }
-        if (!(ok = wait(Q_DSREADY + (j & 1), (uint32_t)((j >> 1) & 1)))) break;
+        if (!(ok = wait(Q_DSREADY, (uint32_t)(j & 1)))) break;
         ptx::tc_fence_after();
         const int sk = j % KSLOTS;
         const uint64_t bk = ptx::launder(ptx::smem_desc_sw128(sbase + DQ_OFF_K + sk * TILE_BYTES, HALF_BYTES, 1024));
-        const uint32_t ds = ptx::launder(tdS + 64 * (j & 1));
+        const uint32_t ds = ptx::launder(tdS);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)  // dQ += dS K (K = keys)
           ptx::mma_ts(tdQ, ds + kk * 8, bk + (uint64_t)((kk * 2048) >> 4), ID_G, (j > 0 || kk > 0) ? 1u : 0u);
         ptx::mma_commit(bar(Q_KEMPTY + sk));
-        ptx::mma_commit(bar(Q_DQDONE + (j & 1)));
+        ptx::mma_commit(bar(Q_DQDONE));
       }
       if (ok) ptx::mma_commit(bar(Q_ODONE));
       ptx::mma_commit(bar(Q_MMADONE));
@@ -550,8 +552,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto wait = [&](int b, uint32_t ph) {
       return __all_sync(0xffffffffu, ptx::mbar_wait(bar(b), ph, G, abort_flag, kDevTimeoutSoftmax));
     };
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
+    bool ok = wait(Q_RES, 0);   // Q and dO resident in shared memory
+    if (ok) {
+      // this warpgroup's half of the thread's Q row (head-dim columns [64 wg, 64 wg + 64)) from
+      // the 128-byte-swizzled tile into TMEM as bf16 pairs: Q columns [32 wg, 32 wg + 32), the
+      // layout the S GEMM reads its A operand in (column c holds elements 2c and 2c + 1)
+      const uint8_t* qrow = smem + OFF_A0 + wg * HALF_BYTES + row * 128;
+      uint32_t qk[32];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) * 16));
+        qk[4 * c] = v.x;
+        qk[4 * c + 1] = v.y;
+        qk[4 * c + 2] = v.z;
+        qk[4 * c + 3] = v.w;
+      }
+      ptx::tmem_st32(tQ + lane_bits + 32 * wg, qk);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar(Q_QTMEM));
+    }
+    for (int j = 0; ok && j < T; ++j) {
       if (!(ok = wait(Q_SFULL, (uint32_t)(j & 1)))) break;
       ptx::tc_fence_after();
       uint32_t r[64];
@@ -587,13 +608,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::f2_unpack(ptx::f2_mul(ptx::f2_pack(pv[2 * c], pv[2 * c + 1]), ptx::f2_pack(y0, y1)), d0, d1);
         pk[c] = ptx::bf16x2(d0, d1);
       }
-      // dS(j) goes to buffer j % 2 once the dQ GEMM of tile j - 2 has read it
-      if (j >= 2 && !(ok = wait(Q_DQDONE + (j & 1), (uint32_t)(((j - 2) >> 1) & 1)))) break;
+      // dS(j) overwrites dS(j-1) once the dQ GEMM of tile j - 1 has read it
+      if (j >= 1 && !(ok = wait(Q_DQDONE, (uint32_t)((j - 1) & 1)))) break;
       ptx::tc_fence_after();
-      ptx::tmem_st32(tdS + lane_bits + 64 * (j & 1) + 32 * wg, pk);
+      ptx::tmem_st32(tdS + lane_bits + 32 * wg, pk);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar(Q_DSREADY + (j & 1)));
+      ptx::mbar_arrive(bar(Q_DSREADY));
     }
     if (ok) ok = __all_sync(0xffffffffu, ptx::mbar_wait(bar(Q_ODONE), 0, G, abort_flag, kDevTimeoutEpilogue));
     if (ok) {
