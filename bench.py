@@ -804,7 +804,7 @@ def our_arm(args, w, ws, rank, local):
         elif not step.joint:
             # heads on either side of a Ulysses head-group boundary, and the last head
             hs = sorted({0, w.Hu - 1, w.Hu, w.H - 1})
-            cpu = oracle_rows_baseline(w, step, hs, 12288, cpu_cores())
+            cpu = oracle_rows_baseline(w, step, hs, 28672, cpu_cores())
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
@@ -871,7 +871,8 @@ def main():
         if args.heads < w.ulysses or args.heads % w.ulysses:
             raise SystemExit(f"--heads must be a positive multiple of {w.ulysses}")
         import dataclasses
-        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
+        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}",
+                                description=f"{w.description}, {args.heads} of its {w.H} heads (profiling case)")
     big = w.N * w.N * w.H > 1e11
     if args.steps is None:
         args.steps = 20 if big else 400
