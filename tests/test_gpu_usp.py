@@ -96,6 +96,29 @@ def test_usp_small_full_rows(dtype, B, H, N, u, r, mode):
     check_out(o, l, ro, rl, dtype, f"{mode} {dtype} B{B} H{H} N{N} u{u} r{r}")
 
 
+@pytest.mark.parametrize("D,misaligned", [(16, False), (40, False), (64, False), (32, True)])
+def test_ring_merge_into_token_layout(D, misaligned):
+    """The materialised forward's ring merge writes the token-sharded out and
+    lse directly; fp32 head dims 16 / 64 (and the default 32) take its
+    vectorised form, 40 and an output pointer off the 16-byte grid its
+    one-element-per-thread form.  Every row against the oracle."""
+    import diffusion_transformer_sequence_gb300 as usp
+    w = wl.custom("mergetok", "f32", 2, 6, 180, D, 3, 2, seed=D + 17)   # Ns = 30, Nr = 90
+    inp = wl.make_inputs(w)
+    stacks = _stacks(w, inp)
+    dev = [t.cuda() for t in stacks]
+    n = int(np.prod(w.stack_shape))
+    raw = torch.full((n + 4,), float("nan"), dtype=torch.float32, device="cuda")
+    out = (raw[1:1 + n] if misaligned else raw[:n]).view(w.stack_shape)
+    lse = torch.full(w.lse_stack_shape, float("nan"), dtype=torch.float32, device="cuda")
+    o, l = usp.attention_fwd(*dev, w.ulysses, w.ring, w.scale, mode="materialised", out=out, lse=lse)
+    assert usp.device_status() == 0
+    outside = torch.cat([raw[:1], raw[1 + n:]]) if misaligned else raw[n:]
+    assert torch.isnan(outside).all(), "the merge wrote outside the output"
+    ro, rl = oracle.usp_forward(*[f64(t) for t in stacks], w.ulysses, w.ring, w.scale)
+    check_out(o, l, ro, rl, "f32", f"merge into token layout D{D} misaligned={misaligned}")
+
+
 def _check_sampled(w, mode, rows_count=4096):
     inp = wl.make_inputs(w)
     stacks = _stacks(w, inp)
