@@ -8,8 +8,9 @@
 // budget), and latency-critical callers that must not call cudaMalloc or
 // cudaFree in their request path because those calls may synchronise the
 // device.  Such callers still pass their inputs and outputs; only the
-// intermediate buffers (head-sharded q/k/v, per-ring-step partial outputs and
-// LSEs, merged head-sharded results) come from here.
+// intermediate buffers (head-sharded q/k/v, and the per-ring-step partial
+// outputs and LSEs -- or, with one ring step, the head-sharded chunk result)
+// come from here.
 //
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes: every
 // GPU that loads the library holds it until the process exits.  Host code may
@@ -17,9 +18,9 @@
 // stand-in object), so the device address is looked up with
 // cudaGetSymbolAddress once per device, with that device current, on the first
 // call made on that device.  That first call should therefore come before any
-// stream capture.  The address is cached with the id of the device's primary
-// context; after a cudaDeviceReset the next call sees a new context id and
-// looks the address up again.  All calls share the one array and it keeps the previous
+// stream capture.  The address is cached with the id of the current context;
+// after a cudaDeviceReset the next call sees a new context id and looks the
+// address up again.  All calls share the one array and it keeps the previous
 // call's contents; nothing in this path needs it zeroed (every byte is written
 // before it is read).  Calls whose executions overlap on the GPU -- on
 // different streams, or from different host threads -- race on the array and
