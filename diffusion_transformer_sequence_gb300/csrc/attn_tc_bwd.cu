@@ -85,9 +85,10 @@ __device__ __forceinline__ int64_t vec_index(const BwdParams& p, int64_t bh, con
   return ((int64_t)t.seg * p.BH + bh) * p.Ns_pad + t.row0 + r;
 }
 
-// Shared memory (both kernels): two resident 128-row tiles A0, A1 (K and V
-// for dK/dV, Q and dO for dQ), STAGES x (two streamed 128-row tiles + two
-// fp32 vectors), then barriers.  Every GEMM is a 128 x 128 (x 128 or 64)
+// Shared memory: two resident 128-row tiles A0, A1 (K and V for dK/dV, Q and
+// dO for dQ); then the dK/dV kernel's STAGES x (two streamed 128-row tiles +
+// two fp32 vectors) and barriers (the dQ kernel's K and V rings are laid out
+// with it, below).  Every GEMM is a 128 x 128 (x 128 or 64)
 // tcgen05.mma: a narrower N costs nearly the same time per 16-deep step
 // (69 against 65 clocks measured at N = 64 and 128), so it halves the rate.
 constexpr int STAGES = 2;
@@ -96,20 +97,17 @@ constexpr int OFF_A1 = TILE_BYTES;
 constexpr int OFF_STAGE = 2 * TILE_BYTES;
 constexpr int STAGE_BYTES = 2 * TILE_BYTES + 2 * VEC_BYTES;
 constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
-enum Bar : int {
-  B_RES = 0,                    // resident tiles landed
-  B_FULL = 1,                   // + stage
-  B_EMPTY = B_FULL + STAGES,    // + stage
-  B_SFULL = B_EMPTY + STAGES,   // S-like GEMM done
-  B_DPFULL,                     // dP-like GEMM done
-  B_PREADY,                     // dK/dV: first half of P^T written to TMEM | dQ: S read (free)
-  B_PREADY2,                    // dK/dV: second half of P^T written
-  B_DSREADY,                    // dS written to TMEM (dK/dV: slot 0; dQ: + dS buffer, so a
-                                //   phase can never be completed twice before it is observed)
-  B_DPFREE = B_DSREADY + 2,     // dQ: dP read (free)
-  B_DQDONE,                     // dQ: + dS buffer, dQ GEMM that read it done
-  B_ODONE = B_DQDONE + 2,
-  B_MMADONE,
+enum Bar : int {  // the dK/dV kernel's barriers
+  B_RES = 0,                    // resident K and V landed
+  B_FULL = 1,                   // + stage: a query tile's Q, dO, L2, Delta landed
+  B_EMPTY = B_FULL + STAGES,    // + stage: the tile's last GEMM (dK) done, stage free
+  B_SFULL = B_EMPTY + STAGES,   // S^T GEMM done
+  B_DPFULL,                     // dP^T GEMM done
+  B_PREADY,                     // first half of P^T written to TMEM (256 arrivals)
+  B_PREADY2,                    // second half of P^T written (256)
+  B_DSREADY,                    // dS^T written to TMEM (256)
+  B_ODONE,                      // the last dV and dK GEMMs done
+  B_MMADONE,                    // every MMA of the CTA done (drain before TMEM is released)
   NUM_BARS
 };
 constexpr int OFF_SLOT = OFF_BAR + NUM_BARS * 8;
@@ -119,7 +117,7 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint32_t stage_addr(uint32_t sbase, int s) { return sbase + OFF_STAGE + s * STAGE_BYTES; }
 
-// Common prologue: barriers and TMEM.  Returns the TMEM base.
+// dK/dV prologue: barriers and TMEM.  Returns the TMEM base.
 __device__ __forceinline__ uint32_t prologue(uint8_t* smem, uint32_t sbase, int warp) {
   auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8 * i; };
   if (threadIdx.x == 0) {
@@ -133,10 +131,6 @@ __device__ __forceinline__ uint32_t prologue(uint8_t* smem, uint32_t sbase, int 
     ptx::mbar_init(bar(B_PREADY), 256);
     ptx::mbar_init(bar(B_PREADY2), 256);
     ptx::mbar_init(bar(B_DSREADY), 256);
-    ptx::mbar_init(bar(B_DSREADY + 1), 256);
-    ptx::mbar_init(bar(B_DPFREE), 256);
-    ptx::mbar_init(bar(B_DQDONE), 1);
-    ptx::mbar_init(bar(B_DQDONE + 1), 1);
     ptx::mbar_init(bar(B_ODONE), 1);
     ptx::mbar_init(bar(B_MMADONE), 1);
     *reinterpret_cast<volatile int*>(smem + OFF_ABORT) = 0;
@@ -400,13 +394,13 @@ constexpr int DQ_OFF_K = 2 * TILE_BYTES;
 constexpr int DQ_OFF_V = DQ_OFF_K + KSLOTS * TILE_BYTES;
 constexpr int DQ_OFF_BAR = DQ_OFF_V + VSLOTS * TILE_BYTES;
 enum DqBar : int {
-  Q_RES = 0,
-  Q_KFULL = 1,
-  Q_KEMPTY = Q_KFULL + KSLOTS,
-  Q_VFULL = Q_KEMPTY + KSLOTS,
-  Q_VEMPTY = Q_VFULL + VSLOTS,
-  Q_SFULL = Q_VEMPTY + VSLOTS,
-  Q_DPFULL,
+  Q_RES = 0,                // resident Q and dO landed
+  Q_KFULL = 1,              // + slot: a K tile landed
+  Q_KEMPTY = Q_KFULL + KSLOTS,  // + slot: free (one elementwise thread, after it saw dQ(j) done)
+  Q_VFULL = Q_KEMPTY + KSLOTS,  // + slot: a V tile landed
+  Q_VEMPTY = Q_VFULL + VSLOTS,  // + slot: free (one elementwise thread, after it saw dP(j) done)
+  Q_SFULL = Q_VEMPTY + VSLOTS,  // S GEMM done
+  Q_DPFULL,                 // dP GEMM done
   Q_SFREE,                  // S(j) read by the warps (256 arrivals)
   Q_DPFREE,                 // dP(j) read (256)
   Q_DSREADY,                // dS(j) written (256)
