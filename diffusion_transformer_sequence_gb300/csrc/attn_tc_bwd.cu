@@ -188,10 +188,10 @@ __device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 4 ? kk * 8 
 //   dK/dV per query tile i:  S^T(i) dP^T(i) | dV(i) S^T(i+1) | dK(i) dP^T(i+1) ...
 //     the warps compute P^T(i) while dP^T(i) runs, dS^T(i) while dV(i) and
 //     S^T(i+1) run.  S^T(i+1) overwrites the columns dV(i) reads P^T(i)
-//     from, so the chain P^T(i) -> dV(i) -> S^T(i+1) -> P^T(i+1) sets the
-//     tile's pace; the warps therefore hand P^T over in two halves (the first
-//     32 query columns of each warpgroup, then the rest) and the first half of
-//     dV(i) runs while they compute the second;
+//     from, so it follows dV(i); the warps hand P^T over in two halves (the
+//     first 32 query columns of each warpgroup, then the rest) and the first
+//     half of dV(i) runs while they compute the second (1-2% faster than one
+//     hand-over; quarters were slower);
 //   dQ per key tile j:  S(j+1) dP(j+1) dQ(j) ...  the warps release S(j) and
 //     dP(j) as soon as they have read them, write dS(j) into TMEM once dQ(j-1)
 //     has read dS(j-1), and release the K and V slots (the tensor core's
