@@ -5,7 +5,9 @@
   forwards and both backward calls, every head against the oracle.
 * A 2^20-token sequence (B1 H2 D128, u2 x r4: 131072 tokens per virtual
   rank), fused and materialised forward, on sampled rows (shard boundaries,
-  tile edges) of both heads against the oracle's unsharded attention.
+  tile edges) of both heads against the oracle's unsharded attention; and
+  its backward (u2 x r1 and u2 x r4, both calls) bitwise equal to the
+  unsharded backward, a property that holds at any size.
 
 One past the grid limit (B*H = 65536) is rejected on the host; that case is
 in test_boundary_cpu.py."""
@@ -82,4 +84,42 @@ def test_million_token_sequence():
         gl = wl.from_token_stack(l).reshape(w.H, w.N)[:, rows.cuda()]
         check_out(go, gl, ro, rl, "bf16", f"N=2^20 {mode}")
         del o, l
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("u,r", [(2, 1), (2, 4)])
+def test_million_token_backward_sharded_bitwise_equals_unsharded(u, r):
+    """At 2^20 tokens (B1 H2 D128) the fp64 oracle's backward is out of reach,
+    so the backward is checked through a property that holds at any size: over
+    whole-tile shards (2^19 or 2^17 rows per virtual rank), both backward calls on
+    the sharded stacks equal the unsharded backward bit for bit given the same
+    out and lse (the USP PR page, Validation and Numerics: the exchange only
+    moves data).  This covers the backward kernels' 64-bit row addressing and
+    their largest per-head loops (8192 query and 8192 key tiles).  Inputs are
+    seeded on the device; no oracle value is involved."""
+    usp = _usp()
+    B, H, N, D = 1, 2, 1 << 20, 128
+    w = wl.custom("n1m_bwd", "bf16", B, H, N, D, u, r, seed=(1 << 20) + 1, backward=True)
+    assert w.Ns % 128 == 0
+    gen = torch.Generator(device="cuda").manual_seed(w.seed)
+    g = {n: torch.randn(B, H, N, D, device="cuda", generator=gen).to(torch.bfloat16)
+         for n in ("q", "k", "v", "dout")}
+    one = {n: wl.to_token_stack(t, 1, 1) for n, t in g.items()}
+    o, l = usp.attention_fwd(one["q"], one["k"], one["v"], 1, 1, w.scale, mode="fused")
+    ref = [wl.from_token_stack(t) for t in
+           usp.attention_bwd(one["q"], one["k"], one["v"], o, l, one["dout"], 1, 1, w.scale, mode="fused")]
+    assert usp.device_status() == 0
+    for name, t in zip(("dq", "dk", "dv"), ref):
+        assert torch.isfinite(t.float()).all() and float(t.float().abs().max()) > 0, f"N=2^20 unsharded {name}"
+    st = {n: wl.to_token_stack(t, u, r) for n, t in g.items()}
+    so, sl = wl.to_token_stack(wl.from_token_stack(o), u, r), wl.to_token_stack(wl.from_token_stack(l), u, r)
+    for mode in ("fused", "materialised"):
+        got = usp.attention_bwd(st["q"], st["k"], st["v"], so, sl, st["dout"], u, r, w.scale, mode=mode)
+        assert usp.device_status() == 0
+        for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+            a = wl.from_token_stack(a)
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), \
+                f"N=2^20 {mode} u{u} r{r}: {name} differs from the unsharded backward " \
+                f"({int((a != b).sum())} elements)"
+        del got
         torch.cuda.empty_cache()
